@@ -1,0 +1,180 @@
+"""fp64 CPU oracle for the fused chunked KL distillation loss.
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers. The product path (the CUDA
+library and its Python binding) never imports, calls or links anything here,
+and nothing here imports the product. Inputs reach both sides from the seeded
+generator, which holds none of this arithmetic.
+
+What it computes follows the pages' statement of the method ("Efficient
+Knowledge Distillation for LLMs: Offline Top-K Logits and a Fused Chunked KL
+Loss"; page "Making knowledge distillation cheap enough to run at scale",
+section "Two system changes"):
+
+* the teacher is an offline cache of its top-K (id, logit) pairs per token
+  (the "Offline distillation" paragraph of that section);
+* the loss is the KL divergence between the teacher distribution and the
+  student's full-vocabulary distribution, whose logits are the student's
+  output projection z = H W^T (the "Fused, chunked KL loss" paragraph; the
+  dense KL is the textbook form those bullets use as the correctness
+  baseline, and the three offline variants are stated to be mathematically
+  equivalent);
+* the closed-form gradient is named but never printed on the pages; it is
+  derived here from the definition.
+
+Readings taken where the pages are silent (each is pinned by a test):
+
+1. Teacher: p_{t,k} = softmax_k(topk_logit_{t,k} / tau), renormalised over the
+   K cached entries (a -inf logit gives p = 0).
+2. Student: log q_{t,v} = z_{t,v}/tau - lse_t with lse_t = log sum_v exp(z_{t,v}/tau),
+   over the FULL vocabulary (not renormalised over the K ids).
+3. Direction: forward KL(p || q), per entry:
+   KL_t = sum_k p_{t,k} (log p_{t,k} - log q_{t, idx_{t,k}}), with 0 log 0 = 0.
+4. No tau^2 factor.
+5. loss = sum_t m_t KL_t / N with N = sum_t m_t (mask m_t in {0,1}); loss = 0
+   when N = 0.
+6. dL/dz_{t,v} = m_t (q_{t,v} - P_{t,v}) / (tau N), where P scatter-adds the
+   K teacher probabilities of row t into a dense vocabulary row (duplicate ids
+   add up). The upstream gradient g = dL_outer/dloss scales it.
+7. dH = G W and dW = G^T H with G = g dL/dz.
+
+The only "blocking" is over rows (tokens), which the definition treats
+independently; no step is fused or reordered.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16/int16 array) to float64:
+    a bf16 value is the upper half of the float32 with the same bits."""
+    b = np.asarray(bits).view(np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def teacher_probs(topk_logit, tau: float) -> np.ndarray:
+    """Reading 1: p_{t,k} = exp(l_{t,k}/tau) / sum_j exp(l_{t,j}/tau)."""
+    a = np.asarray(topk_logit, dtype=np.float64) / tau
+    amax = np.max(a, axis=1, keepdims=True)
+    e = np.exp(a - amax)
+    return e / np.sum(e, axis=1, keepdims=True)
+
+
+def student_logits(H, W) -> np.ndarray:
+    """The student's output projection z = H W^T (dense tokens x vocab grid)."""
+    return np.asarray(H, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+
+
+def student_log_softmax(H, W, tau: float):
+    """Reading 2: returns (log q [T,V], lse [T]) with lse_t = log sum_v e^{z_{t,v}/tau}."""
+    zt = student_logits(H, W) / tau
+    zmax = np.max(zt, axis=1, keepdims=True)
+    lse = zmax[:, 0] + np.log(np.sum(np.exp(zt - zmax), axis=1))
+    return zt - lse[:, None], lse
+
+
+def _xlogx_terms(p: np.ndarray) -> np.ndarray:
+    """p log p with the convention 0 log 0 = 0."""
+    safe = np.where(p > 0, p, 1.0)
+    return np.where(p > 0, p * np.log(safe), 0.0)
+
+
+def token_kl(logq, topk_idx, p) -> np.ndarray:
+    """Reading 3: KL_t = sum_k p_{t,k} (log p_{t,k} - log q_{t, idx_{t,k}})."""
+    logq_at = np.take_along_axis(logq, np.asarray(topk_idx, dtype=np.int64), axis=1)
+    cross = np.where(p > 0, p * logq_at, 0.0)
+    return np.sum(_xlogx_terms(p), axis=1) - np.sum(cross, axis=1)
+
+
+def mask_count(mask) -> int:
+    return int(np.count_nonzero(np.asarray(mask)))
+
+
+def check_indices(topk_idx, V: int) -> None:
+    idx = np.asarray(topk_idx)
+    if idx.size and (idx.min() < 0 or idx.max() >= V):
+        raise ValueError("topk_idx outside [0, V)")
+
+
+def forward(H, W, topk_idx, topk_logit, mask, tau: float):
+    """Returns (loss, lse [T], token_kl [T]) from the dense definition."""
+    check_indices(topk_idx, np.asarray(W).shape[0])
+    logq, lse = student_log_softmax(H, W, tau)
+    p = teacher_probs(topk_logit, tau)
+    kl = token_kl(logq, topk_idx, p)
+    m = np.asarray(mask) != 0
+    n = int(np.count_nonzero(m))
+    loss = float(np.sum(kl[m]) / n) if n else 0.0
+    return loss, lse, kl
+
+
+def dense_teacher(topk_idx, p, V: int) -> np.ndarray:
+    """Reading 6's P: the K teacher probabilities of each row scattered into a
+    dense vocabulary row (the 'dense KL' grid), duplicate ids adding up."""
+    T = p.shape[0]
+    P = np.zeros((T, V), dtype=np.float64)
+    rows = np.repeat(np.arange(T), p.shape[1])
+    np.add.at(P, (rows, np.asarray(topk_idx, dtype=np.int64).ravel()), p.ravel())
+    return P
+
+
+def dense_kl(logq, P) -> np.ndarray:
+    """The pages' dense KL: sum over the whole vocabulary of P (log P - log q)."""
+    return np.sum(_xlogx_terms(P), axis=1) - np.sum(np.where(P > 0, P * logq, 0.0), axis=1)
+
+
+def grad_logits(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss: float = 1.0,
+                n_total: int | None = None) -> np.ndarray:
+    """Reading 6/7: G_{t,v} = g m_t (q_{t,v} - P_{t,v}) / (tau N) for the given rows.
+
+    ``n_total`` is N over the whole batch when the rows passed are a subset."""
+    V = np.asarray(W).shape[0]
+    logq, _ = student_log_softmax(H, W, tau)
+    q = np.exp(logq)
+    P = dense_teacher(topk_idx, teacher_probs(topk_logit, tau), V)
+    m = (np.asarray(mask) != 0).astype(np.float64)
+    n = mask_count(mask) if n_total is None else int(n_total)
+    if n == 0:
+        return np.zeros_like(q)
+    return (q - P) * (grad_loss * m / (tau * n))[:, None]
+
+
+def backward(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss: float = 1.0):
+    """Returns (dH [T,d], dW [V,d]) in fp64: dH = G W, dW = G^T H."""
+    check_indices(topk_idx, np.asarray(W).shape[0])
+    G = grad_logits(H, W, topk_idx, topk_logit, mask, tau, grad_loss)
+    return G @ np.asarray(W, dtype=np.float64), G.T @ np.asarray(H, dtype=np.float64)
+
+
+def lse_rows(H, W, tau: float, rows_per_block: int = 256) -> np.ndarray:
+    """lse_t for every row of H, one block of rows at a time (rows are
+    independent in the definition)."""
+    H = np.asarray(H)
+    out = np.empty(H.shape[0], dtype=np.float64)
+    for r0 in range(0, H.shape[0], rows_per_block):
+        out[r0:r0 + rows_per_block] = student_log_softmax(H[r0:r0 + rows_per_block], W, tau)[1]
+    return out
+
+
+def dW_rows(H, W, topk_idx, topk_logit, mask, tau: float, vocab_rows, lse,
+            grad_loss: float = 1.0) -> np.ndarray:
+    """dW[v, :] = sum_t G_{t,v} H_t for the listed vocabulary rows v, given the
+    full lse [T] (from ``lse_rows``). Same definition as ``backward``,
+    evaluated only on the requested columns of G."""
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    vs = np.asarray(vocab_rows, dtype=np.int64)
+    zt = (H @ W[vs].T) / tau  # [T, |vs|]
+    q = np.exp(zt - np.asarray(lse)[:, None])
+    p = teacher_probs(topk_logit, tau)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    P = np.zeros_like(q)
+    for j, v in enumerate(vs):
+        P[:, j] = np.sum(np.where(idx == v, p, 0.0), axis=1)
+    m = (np.asarray(mask) != 0).astype(np.float64)
+    n = mask_count(mask)
+    if n == 0:
+        return np.zeros((len(vs), H.shape[1]))
+    G = (q - P) * (grad_loss * m / (tau * n))[:, None]
+    return G.T @ H

@@ -1,0 +1,138 @@
+/*
+ * kdkl.h — C ABI of the fused chunked KL distillation loss for GB300 (sm_103a).
+ *
+ * The operation is the one stated in "Efficient Knowledge Distillation for
+ * LLMs: Offline Top-K Logits and a Fused Chunked KL Loss" (page "Making
+ * knowledge distillation cheap enough to run at scale", section "Two system
+ * changes"): a student's output projection z = H W^T over the full
+ * vocabulary, compared by a KL divergence with an offline cache of the
+ * teacher's top-K (id, logit) pairs per token, without ever storing the
+ * tokens x vocabulary logit grid. The backward recomputes the projection
+ * (same section, the fused-chunked bullet; page 4, section "Two systemic
+ * changes", item 2: "the backward pass recomputes each chunk on the fly").
+ *
+ * Definitions (the pages name a closed-form gradient but do not print it):
+ *   p[t,k]   = softmax_k(topk_logit[t,k] / tau)        teacher, renormalised over K
+ *   lse[t]   = log sum_v exp(z[t,v] / tau)             full vocabulary
+ *   KL[t]    = sum_k p[t,k] (log p[t,k] - z[t,idx[t,k]]/tau + lse[t])
+ *   loss     = sum_t m[t] KL[t] / N,  N = sum_t m[t]   (0 when N = 0)
+ *   dL/dz    = m[t] (softmax(z[t]/tau) - P[t]) / (tau N), P = p scattered at idx
+ *   dH = g dL/dz . W,  dW = g (dL/dz)^T . H            (g = upstream gradient)
+ *
+ * Conventions for every call:
+ *   - All arrays are DEVICE pointers, row-major and contiguous, owned by the
+ *     caller. The library never allocates device memory: scratch lives in a
+ *     caller-provided workspace of kd_kl_workspace_size() bytes.
+ *   - bf16 arrays are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous on it and never synchronise the device, except
+ *     kd_kl_check_status() and kd_timing_end(), which say so.
+ *   - Argument errors are returned synchronously and launch nothing.
+ *     Errors found on the device (a topk index outside [0, V), a teacher row
+ *     with no finite logit, a pipeline wait that ran out) are recorded in the
+ *     workspace and read with kd_kl_check_status().
+ *   - Calls sharing one workspace must be ordered on one stream.
+ */
+#ifndef KDKL_H
+#define KDKL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDKL_MAX_K 512 /* largest K the teacher-prep sort handles */
+
+typedef enum {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,  /* null pointer, tau <= 0 or not finite, chunk < 1,
+                              or (device) a teacher row without a finite logit */
+  KD_ERR_SHAPE = 2,        /* T < 0, d < 8, V < 1, K < 1, K > V, K > KDKL_MAX_K,
+                              or a size >= 2^31 */
+  KD_ERR_ALIGNMENT = 3,    /* d % 8 != 0, or H/W/dH/dW/workspace not 16-byte aligned */
+  KD_ERR_INDEX_RANGE = 4,  /* (device) a topk_idx entry outside [0, V) */
+  KD_ERR_WORKSPACE = 5,    /* workspace NULL or smaller than kd_kl_workspace_size() */
+  KD_ERR_CUDA = 6,         /* a CUDA runtime or driver call failed */
+  KD_ERR_TIMEOUT = 7,      /* (device) a bounded pipeline wait ran out; outputs undefined */
+  KD_ERR_UNSUPPORTED = 8   /* the current device is not compute capability 10.3 */
+} kd_status;
+
+typedef struct {
+  int64_t T;          /* tokens (rows of H) */
+  int64_t d;          /* hidden size (columns of H and W); multiple of 8 */
+  int64_t V;          /* vocabulary size (rows of W) */
+  int32_t K;          /* cached teacher entries per token, 1..min(V, KDKL_MAX_K) */
+  float temperature;  /* tau > 0; divides both student and teacher logits */
+  int64_t chunk;      /* token-chunk size of the pages' method: bounds the
+                         backward's gradient-of-logits buffer to chunk x V
+                         bf16 elements (the scheduler may tile that budget as
+                         fewer tokens x more vocabulary; results are the same) */
+} kd_kl_problem;
+
+/* Workspace bytes for kd_kl_forward (which = 0) or kd_kl_backward (which = 1).
+ * Linear in T (no T x V term). Returns 0 if the problem is invalid. */
+size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which);
+
+/* Forward: mean KL loss over unmasked tokens and the per-token logsumexp.
+ *   H          [T, d] bf16        student hidden states
+ *   W          [V, d] bf16        student output projection (LM head)
+ *   topk_idx   [T, K] int32       teacher's cached ids, any order, in [0, V)
+ *   topk_logit [T, K] fp32        teacher's cached logits (-inf allowed, not all)
+ *   mask       [T] uint8 or NULL  nonzero = token counts (NULL: all count)
+ *   loss       [1] fp32 out       sum_t m[t] KL[t] / N (0 when N = 0)
+ *   lse        [T] fp32 out       log sum_v exp(z[t,v]/tau), every row
+ *   token_kl   [T] fp32 out or NULL   KL[t] before masking
+ * The logits z are produced tile by tile inside the SMs and never written to
+ * memory. */
+kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                        const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                        float* loss, float* lse, float* token_kl,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward: gradients of g * loss.
+ *   lse        [T] fp32           from kd_kl_forward on the same inputs
+ *   grad_loss  g                  upstream dL_outer/dloss (host scalar)
+ *   dH         [T, d] bf16 out    overwritten; fp32 accumulation inside, masked rows = 0
+ *   dW         [V, d] fp32 out    overwritten, or added to when accumulate_dW != 0
+ * Each logit tile is recomputed and turned into (softmax - P) in the GEMM
+ * epilogue; the result is kept in a bf16 buffer of at most chunk x V
+ * elements that feeds the dH and dW tensor-core GEMMs. */
+kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                         const float* lse, float grad_loss,
+                         uint16_t* dH, float* dW, int accumulate_dW,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* BLOCKING: synchronises `stream`, then returns the first device-detected
+ * error recorded in `workspace` by the latest call that used it (KD_OK if
+ * none). Each forward/backward call clears the record when it starts. */
+kd_status kd_kl_check_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* kd_status_string(kd_status status);
+
+/* Number of kernels this library has launched in this process (all calls,
+ * all devices). Lets a caller count launches inside a timed region. */
+int64_t kd_launch_count(void);
+
+/* Per-kernel timing. After kd_timing_begin(), every kernel the library
+ * launches is bracketed by CUDA events recorded on its launch stream.
+ * kd_timing_end() is BLOCKING: it synchronises those events, fills up to
+ * `max_entries` rows (one per kernel name, in first-launch order), stores
+ * the row count in *n_entries, and stops recording. */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+} kd_kernel_time;
+
+kd_status kd_timing_begin(void);
+kd_status kd_timing_end(kd_kernel_time* out, int max_entries, int* n_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDKL_H */

@@ -1,0 +1,558 @@
+// C ABI of the fused chunked KL distillation loss: argument checks, the
+// workspace plan, the chunk scheduler and the launch sequence.
+//
+// Forward  (one pass over all tokens; no logits leave the SMs):
+//   teacher_prep -> fwd_lse_gemm -> lse_combine -> loss_finalize
+// Backward (recompute per block of the tokens x vocabulary plane):
+//   teacher_prep -> for each block: bwd_grad_gemm -> dH_gemm -> dW_gemm
+//                -> f32_to_bf16 (dH)
+//
+// The pages ("Efficient Knowledge Distillation for LLMs: Offline Top-K Logits
+// and a Fused Chunked KL Loss", page "Making knowledge distillation cheap
+// enough to run at scale", section "Two system changes") process one chunk of
+// sequence positions at a time so memory grows linearly with the sequence and
+// recompute each chunk in backward. Here `chunk` bounds the one buffer that
+// holds gradients of logits (chunk x V bf16). The forward needs no such
+// buffer at all: its epilogue keeps only three floats per token and split.
+// In backward the scheduler tiles the same budget either as `chunk` tokens by
+// the whole vocabulary, or (when T <= V) all tokens by a vocabulary slab, so
+// that the fp32 read-modify-write lands on the smaller of dW [V,d] and
+// dH [T,d]. Both tilings give the same sums.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/kdkl.h"
+#include "kdkl_internal.h"
+#include "tc_gemm.cuh"
+
+namespace kdkl {
+
+// ------------------------------------------------------------ bookkeeping
+
+namespace {
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<bool> g_timing{false};
+std::mutex g_timing_mu;
+
+struct PendingTiming {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::vector<PendingTiming> g_pending;
+
+}  // namespace
+
+void note_launch_begin(const char* name, cudaStream_t stream, void** token) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  *token = nullptr;
+  if (!g_timing.load(std::memory_order_acquire)) return;
+  auto* p = new PendingTiming{name, nullptr, nullptr};
+  if (cudaEventCreate(&p->start) != cudaSuccess || cudaEventCreate(&p->stop) != cudaSuccess) {
+    delete p;
+    return;
+  }
+  cudaEventRecord(p->start, stream);
+  *token = p;
+}
+
+void note_launch_end(void* token, cudaStream_t stream) {
+  if (!token) return;
+  auto* p = static_cast<PendingTiming*>(token);
+  cudaEventRecord(p->stop, stream);
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_pending.push_back(*p);
+  delete p;
+}
+
+// ------------------------------------------------------------- device info
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;  // int status; int n_count; padding
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+kd_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KD_ERR_CUDA;
+    di.supported = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    di.init = true;
+  }
+  *out = di;
+  return di.supported ? KD_OK : KD_ERR_UNSUPPORTED;
+}
+
+kd_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode ? KD_OK : KD_ERR_CUDA;
+}
+
+// bf16 row-major matrix [outer, inner] with the given row stride (elements),
+// 128-byte swizzle, box of box_inner x box_outer elements. Out-of-range
+// elements of a box read as zero.
+bool encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// -------------------------------------------------------------- planning
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Vocabulary splits per 128-row tile so that (row tiles x splits) units share
+// out evenly over the persistent CTAs: minimises waves x tiles per unit.
+int choose_nsplit(int m_tiles, int n_tiles, int num_sms) {
+  int best = 1;
+  double best_cost = 1e300;
+  const int cap = std::min(n_tiles, 4096);
+  for (int ns = 1; ns <= cap; ++ns) {
+    const int64_t units = (int64_t)m_tiles * ns;
+    const int64_t grid = std::min<int64_t>(units, num_sms);
+    const int64_t waves = ceil_div(units, grid);
+    const int64_t per_unit = ceil_div(n_tiles, ns);
+    const double cost = (double)waves * ((double)per_unit + 0.05);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+struct FwdPlan {
+  int m_tiles, n_tiles, nsplit, grid;
+  size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_bsum, total;
+};
+
+struct BwdPlan {
+  bool vocab_slabs;  // true: blocks are all tokens x a vocabulary slab
+  int64_t Tb, Vb;    // block extent (tokens, vocabulary)
+  int64_t Tb_pad, Vb_pad;
+  int64_t n_tblocks, n_vblocks;
+  size_t off_sidx, off_sp, off_G, off_dH, total;
+};
+
+bool problem_ok(const kd_kl_problem* p) {
+  if (!p) return false;
+  if (p->T < 0 || p->d < 8 || p->V < 1 || p->K < 1) return false;
+  if (p->K > KDKL_MAX_K || (int64_t)p->K > p->V) return false;
+  if (p->T >= (1ll << 31) || p->V >= (1ll << 31) || p->d >= (1ll << 31)) return false;
+  if (p->d % 8 != 0) return false;
+  if (!(p->temperature > 0.f) || !isfinite(p->temperature)) return false;
+  if (p->chunk < 1) return false;
+  return true;
+}
+
+FwdPlan plan_forward(const kd_kl_problem& p, int num_sms) {
+  FwdPlan f{};
+  f.m_tiles = (int)ceil_div(p.T, BM);
+  f.n_tiles = (int)ceil_div(p.V, BN);
+  f.nsplit = p.T > 0 ? choose_nsplit(f.m_tiles, f.n_tiles, num_sms) : 1;
+  f.grid = (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, num_sms);
+  size_t o = kHeaderBytes;
+  const size_t TK = (size_t)p.T * p.K;
+  f.off_sidx = o; o = align256(o + TK * 4);
+  f.off_sp = o; o = align256(o + TK * 4);
+  f.off_ent = o; o = align256(o + (size_t)p.T * 4);
+  f.off_pm = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
+  f.off_ps = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
+  f.off_pd = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
+  f.off_bsum = o; o = align256(o + (size_t)combine_blocks((int)std::max<int64_t>(p.T, 1)) * 8);
+  f.total = o;
+  return f;
+}
+
+BwdPlan plan_backward(const kd_kl_problem& p) {
+  BwdPlan b{};
+  const int64_t T = std::max<int64_t>(p.T, 1);
+  const double budget = (double)p.chunk * (double)p.V;  // gradient-of-logits elements
+  if (T <= p.V) {
+    b.vocab_slabs = true;
+    b.Tb = T;
+    int64_t vb_max = (int64_t)std::min<double>((double)p.V, std::floor(budget / (double)T));
+    vb_max = std::max<int64_t>(vb_max, 256);
+    b.n_vblocks = ceil_div(p.V, vb_max);
+    b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), 64), p.V);
+    b.n_vblocks = ceil_div(p.V, b.Vb);
+    b.n_tblocks = 1;
+  } else {
+    b.vocab_slabs = false;
+    b.Vb = p.V;
+    b.Tb = std::min<int64_t>(round_up(std::min<int64_t>(p.chunk, T), BM), T);
+    b.n_tblocks = ceil_div(T, b.Tb);
+    b.n_vblocks = 1;
+  }
+  b.Tb_pad = round_up(b.Tb, BM);
+  b.Vb_pad = round_up(b.Vb, BN);
+  size_t o = kHeaderBytes;
+  const size_t TK = (size_t)p.T * p.K;
+  b.off_sidx = o; o = align256(o + TK * 4);
+  b.off_sp = o; o = align256(o + TK * 4);
+  b.off_G = o; o = align256(o + (size_t)b.Tb_pad * b.Vb_pad * 2);
+  b.off_dH = o; o = align256(o + (size_t)p.T * p.d * 4);
+  b.total = o;
+  return b;
+}
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+#define KD_CUDA(x)                              \
+  do {                                          \
+    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+}  // namespace kdkl
+
+using namespace kdkl;
+
+// ------------------------------------------------------------------- C ABI
+
+extern "C" {
+
+const char* kd_status_string(kd_status s) {
+  switch (s) {
+    case KD_OK: return "KD_OK";
+    case KD_ERR_INVALID_ARG: return "KD_ERR_INVALID_ARG";
+    case KD_ERR_SHAPE: return "KD_ERR_SHAPE";
+    case KD_ERR_ALIGNMENT: return "KD_ERR_ALIGNMENT";
+    case KD_ERR_INDEX_RANGE: return "KD_ERR_INDEX_RANGE";
+    case KD_ERR_WORKSPACE: return "KD_ERR_WORKSPACE";
+    case KD_ERR_CUDA: return "KD_ERR_CUDA";
+    case KD_ERR_TIMEOUT: return "KD_ERR_TIMEOUT";
+    case KD_ERR_UNSUPPORTED: return "KD_ERR_UNSUPPORTED";
+  }
+  return "KD_ERR_UNKNOWN";
+}
+
+int64_t kd_launch_count(void) { return g_launches.load(); }
+
+size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which) {
+  if (!problem_ok(prob)) return 0;
+  if (which == 0) {
+    DeviceInfo di;
+    const int sms = (device_info(&di) == KD_OK) ? di.num_sms : 148;
+    // The split count depends on the SM count; size for the larger of the
+    // device's plan and a 1-split plan so the answer is safe either way.
+    return std::max(plan_forward(*prob, sms).total, plan_forward(*prob, 1).total);
+  }
+  if (which == 1) return plan_backward(*prob).total;
+  return 0;
+}
+
+static kd_status validate_common(const kd_kl_problem* prob, const void* H, const void* W,
+                                 const void* idx, const void* logit, const void* workspace) {
+  if (!prob) return KD_ERR_INVALID_ARG;
+  if (prob->T < 0 || prob->d < 8 || prob->V < 1 || prob->K < 1 || prob->K > KDKL_MAX_K ||
+      (int64_t)prob->K > prob->V || prob->T >= (1ll << 31) || prob->V >= (1ll << 31) ||
+      prob->d >= (1ll << 31))
+    return KD_ERR_SHAPE;
+  if (!(prob->temperature > 0.f) || !isfinite(prob->temperature) || prob->chunk < 1)
+    return KD_ERR_INVALID_ARG;
+  if (prob->d % 8 != 0) return KD_ERR_ALIGNMENT;
+  if (!workspace) return KD_ERR_WORKSPACE;
+  if (prob->T > 0 && (!H || !idx || !logit)) return KD_ERR_INVALID_ARG;
+  if (!W) return KD_ERR_INVALID_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(workspace, 16)) return KD_ERR_ALIGNMENT;
+  if (!aligned(idx, 4) || !aligned(logit, 4)) return KD_ERR_ALIGNMENT;
+  return KD_OK;
+}
+
+kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                        const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                        float* loss, float* lse, float* token_kl, void* workspace,
+                        size_t workspace_bytes, void* stream_ptr) {
+  kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
+  if (st != KD_OK) return st;
+  if (!loss || (prob->T > 0 && !lse)) return KD_ERR_INVALID_ARG;
+  if (!aligned(loss, 4) || !aligned(lse, 4) || !aligned(token_kl, 4)) return KD_ERR_ALIGNMENT;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KD_OK) return st;
+  if ((st = get_encoder()) != KD_OK) return st;
+  const kd_kl_problem& p = *prob;
+  const FwdPlan f = plan_forward(p, di.num_sms);
+  if (workspace_bytes < f.total) return KD_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  int* status = at<int>(workspace, 0);
+  int* n_count = status + 1;
+  KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
+  if (p.T == 0) {
+    KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
+    return KD_OK;
+  }
+  const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
+  const float inv_tau = 1.0f / p.temperature;
+  const float cl2 = 1.4426950408889634f * inv_tau;
+  int32_t* sidx = at<int32_t>(workspace, f.off_sidx);
+  float* sp = at<float>(workspace, f.off_sp);
+  float* ent = at<float>(workspace, f.off_ent);
+
+  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, T, K, V, inv_tau, sidx, sp, ent, n_count,
+                              status, stream));
+
+  CUtensorMap tmH, tmW;
+  if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW, W, d, V, d, BK, BN))
+    return KD_ERR_CUDA;
+  GemmShape sh{};
+  sh.m_tiles = f.m_tiles;
+  sh.n_tiles = f.n_tiles;
+  sh.nsplit = f.nsplit;
+  sh.units = f.m_tiles * f.nsplit;
+  sh.k_blocks = (int)ceil_div(d, BK);
+  EpiParams ep{};
+  ep.sidx = sidx;
+  ep.sp = sp;
+  ep.K = K;
+  ep.T = T;
+  ep.row0 = 0;
+  ep.rows = T;
+  ep.col0 = 0;
+  ep.cols = V;
+  ep.cl2 = cl2;
+  ep.pm = at<float>(workspace, f.off_pm);
+  ep.ps = at<float>(workspace, f.off_ps);
+  ep.pd = at<float>(workspace, f.off_pd);
+  KD_CUDA(launch_gemm(GEMM_FWD_LSE, tmH, tmW, sh, ep, status, f.grid, stream));
+
+  double* bsum = at<double>(workspace, f.off_bsum);
+  KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, cl2, inv_tau, lse,
+                             token_kl, bsum, stream));
+  KD_CUDA(launch_loss_finalize(bsum, combine_blocks(T), n_count, loss, stream));
+  return KD_OK;
+}
+
+kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                         const float* lse, float grad_loss, uint16_t* dH, float* dW,
+                         int accumulate_dW, void* workspace, size_t workspace_bytes,
+                         void* stream_ptr) {
+  kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
+  if (st != KD_OK) return st;
+  if (!dW || (prob->T > 0 && (!lse || !dH))) return KD_ERR_INVALID_ARG;
+  if (!isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
+  if (!aligned(dH, 16) || !aligned(dW, 16) || !aligned(lse, 4)) return KD_ERR_ALIGNMENT;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KD_OK) return st;
+  if ((st = get_encoder()) != KD_OK) return st;
+  const kd_kl_problem& p = *prob;
+  const BwdPlan b = plan_backward(p);
+  if (workspace_bytes < b.total) return KD_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  int* status = at<int>(workspace, 0);
+  int* n_count = status + 1;
+  KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
+  if (p.T == 0) {
+    if (!accumulate_dW) KD_CUDA(cudaMemsetAsync(dW, 0, (size_t)p.V * p.d * 4, stream));
+    return KD_OK;
+  }
+  const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
+  const float inv_tau = 1.0f / p.temperature;
+  const float cl2 = 1.4426950408889634f * inv_tau;
+  int32_t* sidx = at<int32_t>(workspace, b.off_sidx);
+  float* sp = at<float>(workspace, b.off_sp);
+  uint16_t* Gbuf = at<uint16_t>(workspace, b.off_G);
+  float* dH_acc = at<float>(workspace, b.off_dH);
+
+  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, T, K, V, inv_tau, sidx, sp, nullptr,
+                              n_count, status, stream));
+
+  CUtensorMap tmH_K, tmW_K, tmW_MN, tmH_MN;
+  if (!encode_bf16_2d(&tmH_K, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW_K, W, d, V, d, BK, BN) ||
+      !encode_bf16_2d(&tmW_MN, W, d, V, d, 64, BK) || !encode_bf16_2d(&tmH_MN, H, d, T, d, 64, BK))
+    return KD_ERR_CUDA;
+
+  const int dn_tiles = (int)ceil_div(d, BN);
+  for (int64_t tb = 0; tb < b.n_tblocks; ++tb) {
+    const int row0 = (int)(tb * b.Tb);
+    const int rows = (int)std::min<int64_t>(b.Tb, p.T - row0);
+    for (int64_t vb = 0; vb < b.n_vblocks; ++vb) {
+      const int col0 = (int)(vb * b.Vb);
+      const int cols = (int)std::min<int64_t>(b.Vb, p.V - col0);
+      if (cols <= 0 || rows <= 0) continue;
+
+      // 1) recompute the logits of the block and store (softmax - P) * m g / (tau N)
+      {
+        GemmShape sh{};
+        sh.m_tiles = (int)ceil_div(rows, BM);
+        sh.n_tiles = (int)ceil_div(cols, BN);
+        sh.nsplit = choose_nsplit(sh.m_tiles, sh.n_tiles, di.num_sms);
+        sh.units = sh.m_tiles * sh.nsplit;
+        sh.k_blocks = (int)ceil_div(d, BK);
+        sh.a_m0 = row0;
+        sh.b_n0 = col0;
+        EpiParams ep{};
+        ep.sidx = sidx;
+        ep.sp = sp;
+        ep.K = K;
+        ep.T = T;
+        ep.row0 = row0;
+        ep.rows = rows;
+        ep.col0 = col0;
+        ep.cols = cols;
+        ep.cl2 = cl2;
+        ep.lse = lse;
+        ep.mask = mask;
+        ep.n_count = n_count;
+        ep.g_over_tau = grad_loss * inv_tau;
+        ep.G = Gbuf;
+        ep.ldg = b.Vb_pad;
+        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
+        KD_CUDA(launch_gemm(GEMM_BWD_GRAD, tmH_K, tmW_K, sh, ep, status, grid, stream));
+      }
+      // 2) dH[rows] (+)= G . W[cols]
+      {
+        CUtensorMap tmG_K;
+        if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM)) return KD_ERR_CUDA;
+        GemmShape sh{};
+        sh.m_tiles = (int)ceil_div(rows, BM);
+        sh.n_tiles = dn_tiles;
+        sh.nsplit = dn_tiles;
+        sh.units = sh.m_tiles * sh.nsplit;
+        sh.k_blocks = (int)ceil_div(cols, BK);
+        sh.b_k0 = col0;
+        EpiParams ep{};
+        ep.out = dH_acc + (int64_t)row0 * d;
+        ep.ldo = d;
+        ep.out_rows = rows;
+        ep.out_cols = d;
+        ep.accumulate = vb > 0 ? 1 : 0;
+        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
+        KD_CUDA(launch_gemm(GEMM_DH, tmG_K, tmW_MN, sh, ep, status, grid, stream));
+      }
+      // 3) dW[cols] (+)= G^T . H[rows]
+      {
+        CUtensorMap tmG_MN;
+        if (!encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK)) return KD_ERR_CUDA;
+        GemmShape sh{};
+        sh.m_tiles = (int)ceil_div(cols, BM);
+        sh.n_tiles = dn_tiles;
+        sh.nsplit = dn_tiles;
+        sh.units = sh.m_tiles * sh.nsplit;
+        sh.k_blocks = (int)ceil_div(rows, BK);
+        sh.b_k0 = row0;
+        EpiParams ep{};
+        ep.out = dW + (int64_t)col0 * d;
+        ep.ldo = d;
+        ep.out_rows = cols;
+        ep.out_cols = d;
+        ep.accumulate = (accumulate_dW || tb > 0) ? 1 : 0;
+        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
+        KD_CUDA(launch_gemm(GEMM_DW, tmG_MN, tmH_MN, sh, ep, status, grid, stream));
+      }
+    }
+  }
+  KD_CUDA(launch_f32_to_bf16(dH_acc, dH, (long long)p.T * p.d, di.num_sms, stream));
+  return KD_OK;
+}
+
+kd_status kd_kl_check_status(void* workspace, void* stream_ptr) {
+  if (!workspace) return KD_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int code = 0;
+  if (cudaMemcpyAsync(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return KD_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KD_ERR_CUDA;
+  switch (code) {
+    case 0: return KD_OK;
+    case DEV_ERR_INVALID_ARG: return KD_ERR_INVALID_ARG;
+    case DEV_ERR_INDEX_RANGE: return KD_ERR_INDEX_RANGE;
+    case DEV_ERR_TIMEOUT: return KD_ERR_TIMEOUT;
+    default: return KD_ERR_CUDA;
+  }
+}
+
+kd_status kd_timing_begin(void) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing.store(true, std::memory_order_release);
+  return KD_OK;
+}
+
+kd_status kd_timing_end(kd_kernel_time* out, int max_entries, int* n_entries) {
+  g_timing.store(false, std::memory_order_release);
+  std::vector<PendingTiming> pend;
+  {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    pend.swap(g_pending);
+  }
+  std::vector<kd_kernel_time> rows;
+  kd_status st = KD_OK;
+  for (auto& p : pend) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, p.start, p.stop) != cudaSuccess)
+      st = KD_ERR_CUDA;
+    cudaEventDestroy(p.start);
+    cudaEventDestroy(p.stop);
+    auto it = std::find_if(rows.begin(), rows.end(),
+                           [&](const kd_kernel_time& r) { return strcmp(r.name, p.name) == 0; });
+    if (it == rows.end()) {
+      kd_kernel_time r{};
+      snprintf(r.name, sizeof(r.name), "%s", p.name);
+      rows.push_back(r);
+      it = rows.end() - 1;
+    }
+    it->launches += 1;
+    it->total_ms += ms;
+  }
+  const int n = (int)std::min<size_t>(rows.size(), (size_t)std::max(max_entries, 0));
+  for (int i = 0; i < n && out; ++i) out[i] = rows[i];
+  if (n_entries) *n_entries = (int)rows.size();
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace kdkl {
+
+struct GemmShape;
+struct EpiParams;
+
+// Launch bookkeeping: counts every kernel launch and, while timing is on,
+// brackets it with CUDA events on its stream.
+void note_launch_begin(const char* name, cudaStream_t stream, void** token);
+void note_launch_end(void* token, cudaStream_t stream);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                          size_t smem, cudaStream_t stream, Args&&... args) {
+  void* token = nullptr;
+  note_launch_begin(name, stream, &token);
+  kern<<<grid, block, smem, stream>>>(std::forward<Args>(args)...);
+  const cudaError_t e = cudaGetLastError();
+  note_launch_end(token, stream);
+  return e;
+}
+
+// kernels_small.cu
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
+                                int K, int V, float inv_tau, int32_t* sidx, float* sp, float* ent,
+                                int* n_count, int* status, cudaStream_t stream);
+int combine_blocks(int T);
+cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
+                               const float* ent, const uint8_t* mask, float cl2, float inv_tau,
+                               float* lse, float* token_kl, double* block_sums,
+                               cudaStream_t stream);
+cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,
+                                 float* loss, cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
+                               cudaStream_t stream);
+
+// kernels_gemm.cu — tcgen05 GEMMs (see tc_gemm.cuh for the epilogues)
+enum GemmKind {
+  GEMM_FWD_LSE = 0,   // A = H (K-major), B = W (K-major), online logsumexp + gather
+  GEMM_BWD_GRAD = 1,  // A = H (K-major), B = W (K-major), softmax - P into the bf16 buffer
+  GEMM_DH = 2,        // A = G (K-major), B = W (MN-major), fp32 out
+  GEMM_DW = 3         // A = G (MN-major), B = H (MN-major), fp32 out
+};
+cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const GemmShape& sh, const EpiParams& ep, int* status, int grid,
+                        cudaStream_t stream);
+
+}  // namespace kdkl

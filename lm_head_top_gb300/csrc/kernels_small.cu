@@ -1,0 +1,222 @@
+// Bandwidth-light kernels around the tensor-core GEMMs:
+//   teacher_prep   per token: validate ids, teacher softmax over the K cached
+//                  logits, entropy term, sort (id, p) by id, count the mask.
+//   lse_combine    per token: merge the vocabulary-split partials into lse and
+//                  KL, plus a per-block sum of m_t KL_t (fp64).
+//   loss_finalize  one block: ordered sum of the block sums / N.
+//   f32_to_bf16    dH accumulator to bf16 (round to nearest even).
+//
+// Teacher distribution and KL from "Efficient Knowledge Distillation for
+// LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", page "Making
+// knowledge distillation cheap enough to run at scale", section "Two system
+// changes" (top-100 cache per position; the sparse teacher of the
+// forward-chunked and fused variants).
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kdkl_internal.h"
+#include "tc_primitives.cuh"
+
+namespace kdkl {
+
+constexpr int PREP_WARPS = 8;
+
+// One warp per token row. Dynamic shared memory: PREP_WARPS * p2 * 8 bytes.
+__global__ void __launch_bounds__(PREP_WARPS * 32)
+    teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logit,
+                        const uint8_t* __restrict__ mask, int T, int K, int p2, int V, float inv_tau,
+                        int32_t* __restrict__ sidx, float* __restrict__ sp,
+                        float* __restrict__ ent, int* n_count, int* status) {
+  extern __shared__ uint8_t prep_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* keys = reinterpret_cast<int*>(prep_smem) + warp * p2;
+  float* vals = reinterpret_cast<float*>(prep_smem + (size_t)PREP_WARPS * p2 * 4) + warp * p2;
+  const int t = blockIdx.x * PREP_WARPS + warp;
+  __shared__ int block_count;
+  if (threadIdx.x == 0) block_count = 0;
+  __syncthreads();
+
+  if (t < T) {
+    const int32_t* irow = idx + (long long)t * K;
+    const float* lrow = logit + (long long)t * K;
+    // max of a = logit / tau; validate ids and logits
+    float amax = -INFINITY;
+    bool bad_id = false, bad_logit = false;
+    for (int k = lane; k < K; k += 32) {
+      const int id = __ldg(irow + k);
+      const float a = __ldg(lrow + k) * inv_tau;
+      bad_id |= (id < 0 || id >= V);
+      bad_logit |= (a != a) || (a == INFINITY);
+      amax = fmaxf(amax, a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (__any_sync(0xffffffffu, bad_id) && lane == 0) record_error(status, DEV_ERR_INDEX_RANGE);
+    const bool no_finite = !(amax > -INFINITY);
+    if ((__any_sync(0xffffffffu, bad_logit) || no_finite) && lane == 0)
+      record_error(status, DEV_ERR_INVALID_ARG);
+    // sum of exp(a - max)
+    float sum = 0.f;
+    for (int k = lane; k < K; k += 32) sum += expf(__ldg(lrow + k) * inv_tau - amax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float log_sum = logf(sum);
+    // p, entropy term sum p log p, and the (id, p) pairs to sort
+    float h = 0.f;
+    for (int k = lane; k < p2; k += 32) {
+      if (k < K) {
+        const float a = __ldg(lrow + k) * inv_tau - amax;  // <= 0 or -inf
+        const float p = no_finite ? 0.f : expf(a) / sum;
+        if (p > 0.f) h += p * (a - log_sum);
+        keys[k] = __ldg(irow + k);
+        vals[k] = p;
+      } else {
+        keys[k] = 0x7fffffff;
+        vals[k] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    __syncwarp();
+    // bitonic sort of p2 (power of two) pairs, ascending by id
+    for (int size = 2; size <= p2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = lane; i < (p2 >> 1); i += 32) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool ascending = (lo & size) == 0;
+          const int klo = keys[lo], khi = keys[hi];
+          if ((klo > khi) == ascending) {
+            keys[lo] = khi;
+            keys[hi] = klo;
+            const float vlo = vals[lo];
+            vals[lo] = vals[hi];
+            vals[hi] = vlo;
+          }
+        }
+        __syncwarp();
+      }
+    }
+    int32_t* so = sidx + (long long)t * K;
+    float* po = sp + (long long)t * K;
+    for (int k = lane; k < K; k += 32) {
+      so[k] = keys[k];
+      po[k] = vals[k];
+    }
+    if (lane == 0) {
+      if (ent) ent[t] = h;
+      if (mask == nullptr || mask[t] != 0) atomicAdd(&block_count, 1);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && block_count) atomicAdd(n_count, block_count);
+}
+
+constexpr int COMBINE_THREADS = 256;
+
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                       const float* __restrict__ pd, int nsplit, int T,
+                       const float* __restrict__ ent, const uint8_t* __restrict__ mask, float cl2,
+                       float inv_tau, float* __restrict__ lse, float* __restrict__ token_kl,
+                       double* __restrict__ block_sums) {
+  const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  if (t < T) {
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + t]);
+    float S = 0.f, D = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const long long o = (long long)s * T + t;
+      S += ps[o] * exp2f((pm[o] - M) * cl2);
+      D += pd[o];
+    }
+    const float l = M * inv_tau + logf(S);
+    const float kl = ent[t] - D * inv_tau + l;
+    lse[t] = l;
+    if (token_kl) token_kl[t] = kl;
+    if (mask == nullptr || mask[t] != 0) contrib = (double)kl;
+  }
+  // fixed-shape tree reduction: deterministic
+  __shared__ double red[COMBINE_THREADS];
+  red[threadIdx.x] = contrib;
+  __syncthreads();
+  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) block_sums[blockIdx.x] = red[0];
+}
+
+__global__ void __launch_bounds__(1024)
+    loss_finalize_kernel(const double* __restrict__ block_sums, int nblocks,
+                         const int* __restrict__ n_count, float* __restrict__ loss) {
+  __shared__ double red[1024];
+  double a = 0.0;
+  for (int i = threadIdx.x; i < nblocks; i += 1024) a += block_sums[i];
+  red[threadIdx.x] = a;
+  __syncthreads();
+  for (int w = 512; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int n = *n_count;
+    loss[0] = n > 0 ? (float)(red[0] / (double)n) : 0.f;
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
+                                   long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = in[i];
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// ------------------------------------------------------------ host launchers
+
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
+                                int K, int V, float inv_tau, int32_t* sidx, float* sp, float* ent,
+                                int* n_count, int* status, cudaStream_t stream) {
+  int p2 = 1;
+  while (p2 < K) p2 <<= 1;
+  if (p2 < 2) p2 = 2;
+  const size_t smem = (size_t)PREP_WARPS * p2 * 8;
+  const int blocks = (T + PREP_WARPS - 1) / PREP_WARPS;
+  return launch_kernel("teacher_prep", teacher_prep_kernel, dim3(blocks), dim3(PREP_WARPS * 32),
+                       smem, stream, idx, logit, mask, T, K, p2, V, inv_tau, sidx, sp, ent,
+                       n_count, status);
+}
+
+int combine_blocks(int T) { return (T + COMBINE_THREADS - 1) / COMBINE_THREADS; }
+
+cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
+                               const float* ent, const uint8_t* mask, float cl2, float inv_tau,
+                               float* lse, float* token_kl, double* block_sums,
+                               cudaStream_t stream) {
+  return launch_kernel("lse_combine", lse_combine_kernel, dim3(combine_blocks(T)),
+                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nsplit, T, ent, mask, cl2,
+                       inv_tau, lse, token_kl, block_sums);
+}
+
+cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,
+                                 float* loss, cudaStream_t stream) {
+  return launch_kernel("loss_finalize", loss_finalize_kernel, dim3(1), dim3(1024), 0, stream,
+                       block_sums, nblocks, n_count, loss);
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
+                               cudaStream_t stream) {
+  const long long n4 = n / 4;  // n is a multiple of 8 (d % 8 == 0)
+  long long blocks = (n4 + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel("f32_to_bf16", f32_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                       stream, reinterpret_cast<const float4*>(in), reinterpret_cast<uint2*>(out),
+                       n4);
+}
+
+}  // namespace kdkl

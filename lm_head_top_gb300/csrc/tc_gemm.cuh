@@ -1,0 +1,406 @@
+// Persistent, warp-specialised tcgen05 GEMM for the fused KL loss, with the
+// three epilogues the method needs:
+//
+//   EPI_LSE   forward: logits tile S = H_tile . W_tile^T lives only in TMEM;
+//             each epilogue thread owns one token row and folds the tile into
+//             a running max / sum of exp2 (the logsumexp) and into
+//             sum_k p_k z[idx_k] for the teacher ids that fall in the tile.
+//             Writes one (max, sum, dot) partial per (row, vocab split).
+//   EPI_GRAD  backward: recompute S, form (softmax - P) * m / (tau N) * g in
+//             the epilogue and store it as bf16 into the chunk buffer.
+//   EPI_STORE plain fp32 output (dH and dW GEMMs), store or add.
+//
+// Roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Tiles are 128 x 256 with a 64-deep K step, 4 shared-memory stages, and two
+// 256-column fp32 accumulators in TMEM so the epilogue of one tile overlaps
+// the MMAs of the next.
+//
+// Source of the method: "Efficient Knowledge Distillation for LLMs: Offline
+// Top-K Logits and a Fused Chunked KL Loss", page "Making knowledge
+// distillation cheap enough to run at scale", section "Two system changes"
+// (fused, chunked KL: project a chunk, fold it into the running loss, discard
+// it; recompute in backward).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "tc_primitives.cuh"
+
+namespace kdkl {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int GEMM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256;
+// MN-major operands arrive as 64-element-wide atoms of BK rows each.
+constexpr uint32_t MN_ATOM_BYTES = BK * 128;
+
+enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2 };
+
+// Work decomposition: `units` = m_tiles * nsplit; unit u covers m-tile u / nsplit
+// and a contiguous range of n-tiles (split u % nsplit of n_tiles).
+struct GemmShape {
+  int m_tiles, n_tiles, nsplit, units;
+  int k_blocks;
+  int a_m0, a_k0;  // A coordinate offsets (rows M / reduction K)
+  int b_n0, b_k0;  // B coordinate offsets (rows N / reduction K)
+};
+
+struct EpiParams {
+  // EPI_LSE and EPI_GRAD
+  const int32_t* sidx;  // [T, K] teacher ids sorted ascending per row
+  const float* sp;      // [T, K] teacher probabilities in the same order
+  int K;
+  int T;
+  int row0;     // first token row of this launch (EPI_GRAD)
+  int rows;     // token rows in this launch
+  int col0;     // first vocabulary id of this launch
+  int cols;     // vocabulary columns in this launch
+  float cl2;    // log2(e) / tau
+  // EPI_LSE
+  float* pm;  // [nsplit, T] running max of z
+  float* ps;  // [nsplit, T] sum of exp2((z - max) * cl2)
+  float* pd;  // [nsplit, T] sum_k p_k z[idx_k]
+  // EPI_GRAD
+  const float* lse;
+  const uint8_t* mask;  // may be null (all tokens count)
+  const int* n_count;   // number of counted tokens N
+  float g_over_tau;
+  uint16_t* G;   // bf16 bits, [rows_pad, ldg]
+  int64_t ldg;
+  // EPI_STORE
+  float* out;
+  int64_t ldo;
+  int out_rows, out_cols;
+  int accumulate;
+};
+
+__device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
+                                            int& ne) {
+  m = u / sh.nsplit;
+  s = u - m * sh.nsplit;
+  nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
+  ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
+}
+
+// First position in the sorted id row whose id is >= v (K when none).
+__device__ __forceinline__ int lower_bound_row(const int32_t* row, int K, int v) {
+  int lo = 0, hi = K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(row + mid) < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmShape sh, const EpiParams ep, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+        int m, s, nb, ne;
+        unit_coords(sh, u, m, s, nb, ne);
+        for (int n = nb; ok && n < ne; ++n) {
+          for (int kb = 0; kb < sh.k_blocks; ++kb) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t a_dst = smem_u32(sA + stage * A_STAGE_BYTES);
+            const uint32_t b_dst = smem_u32(sB + stage * B_STAGE_BYTES);
+            const int kc = kb * BK;
+            if (!A_MN) {
+              tma_load_2d(a_dst, &tmA, fb, sh.a_k0 + kc, sh.a_m0 + m * BM);
+            } else {
+#pragma unroll
+              for (int a = 0; a < BM / 64; ++a)
+                tma_load_2d(a_dst + a * MN_ATOM_BYTES, &tmA, fb, sh.a_m0 + m * BM + 64 * a,
+                            sh.a_k0 + kc);
+            }
+            if (!B_MN) {
+              tma_load_2d(b_dst, &tmB, fb, sh.b_k0 + kc, sh.b_n0 + n * BN);
+            } else {
+#pragma unroll
+              for (int a = 0; a < BN / 64; ++a)
+                tma_load_2d(b_dst + a * MN_ATOM_BYTES, &tmB, fb, sh.b_n0 + n * BN + 64 * a,
+                            sh.b_k0 + kc);
+            }
+            ++fills;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Teardown: every issued copy must have landed before the CTA exits.
+      for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f)
+        mbar_drain_bounded(full_bar((int)(f % STAGES)), (uint32_t)((f / STAGES) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+        int m, s, nb, ne;
+        unit_coords(sh, u, m, s, nb, ne);
+        for (int n = nb; ok && n < ne; ++n) {
+          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < sh.k_blocks; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * B_STAGE_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = A_MN ? sdesc_sw128(a_base + k * 2048, MN_ATOM_BYTES, 1024)
+                                       : sdesc_sw128(a_base + k * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, MN_ATOM_BYTES, 1024)
+                                       : sdesc_sw128(b_base + k * 32, 16, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit(tfull_bar(acc));
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      // Teardown: all MMAs issued by this thread complete before TMEM is freed.
+      tc_commit(drain_bar);
+      mbar_drain_bounded(drain_bar, 0);
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+      int m, s, nb, ne;
+      unit_coords(sh, u, m, s, nb, ne);
+      const int r = m * BM + r_in_tile;  // row within this launch
+      // per-unit row state
+      float run_max = -INFINITY, run_sum = 0.f, dot = 0.f;
+      float lse2 = 0.f, scale = 0.f;
+      int cursor = ep.K, cur_id = 0x7fffffff;
+      const int32_t* id_row = nullptr;
+      const float* p_row = nullptr;
+      bool row_ok = false;
+      if (EPI == EPI_LSE || EPI == EPI_GRAD) {
+        row_ok = r < ep.rows;
+        if (row_ok) {
+          const long long tok = (long long)ep.row0 + r;
+          id_row = ep.sidx + tok * ep.K;
+          p_row = ep.sp + tok * ep.K;
+          cursor = lower_bound_row(id_row, ep.K, ep.col0 + nb * BN);
+          cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
+          if (EPI == EPI_GRAD) {
+            lse2 = __ldg(ep.lse + tok) * 1.4426950408889634f;
+            const int n = *ep.n_count;
+            const bool counted = ep.mask == nullptr || __ldg(ep.mask + tok) != 0;
+            scale = (counted && n > 0) ? ep.g_over_tau / (float)n : 0.f;
+          }
+        }
+      }
+      for (int n = nb; n < ne; ++n) {
+        bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + lane_off + (uint32_t)(acc * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int cl = n * BN + c * 32;  // column within this launch
+          if (EPI == EPI_LSE || EPI == EPI_GRAD) {
+            if (cl >= ep.cols) break;  // warp-uniform
+          } else {
+            if (cl >= ep.out_cols) break;
+          }
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          if (EPI == EPI_LSE) {
+            const int vid0 = ep.col0 + cl;
+            if (cl + 32 > ep.cols) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (cl + j >= ep.cols) v[j] = -INFINITY;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            const float nm = fmaxf(run_max, mx);
+            const float nmc = nm * ep.cl2;
+            float acc_s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc_s += ex2_approx(fmaf(v[j], ep.cl2, -nmc));
+            run_sum = fmaf(run_sum, ex2_approx((run_max - nm) * ep.cl2), acc_s);
+            run_max = nm;
+            if (row_ok) {
+              const int vend = ep.col0 + min(cl + 32, ep.cols);
+              while (cur_id < vend) {
+                if (cur_id >= vid0) dot = fmaf(__ldg(p_row + cursor), select32(v, cur_id - vid0), dot);
+                ++cursor;
+                cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
+              }
+            }
+          } else if (EPI == EPI_GRAD) {
+            const int vid0 = ep.col0 + cl;
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = ex2_approx(fmaf(v[j], ep.cl2, -lse2));
+            if (row_ok) {
+              const int vend = ep.col0 + min(cl + 32, ep.cols);
+              while (cur_id < vend) {
+                if (cur_id >= vid0) {
+                  const float pk = __ldg(p_row + cursor);
+                  const int jj = cur_id - vid0;
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) g[j] = (j == jj) ? g[j] - pk : g[j];
+                }
+                ++cursor;
+                cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
+              }
+              uint4* dst = reinterpret_cast<uint4*>(ep.G + (long long)r * ep.ldg + cl);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 w;
+                w.x = pack_bf16x2(g[8 * j + 0] * scale, g[8 * j + 1] * scale);
+                w.y = pack_bf16x2(g[8 * j + 2] * scale, g[8 * j + 3] * scale);
+                w.z = pack_bf16x2(g[8 * j + 4] * scale, g[8 * j + 5] * scale);
+                w.w = pack_bf16x2(g[8 * j + 6] * scale, g[8 * j + 7] * scale);
+                dst[j] = w;
+              }
+            }
+          } else {  // EPI_STORE
+            if (r < ep.out_rows) {
+              float* dst = ep.out + (long long)r * ep.ldo + cl;
+              const int nvalid = min(32, ep.out_cols - cl);  // multiple of 4
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (4 * j < nvalid) {
+                  float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                  if (ep.accumulate) {
+                    const float4 prev = *reinterpret_cast<const float4*>(dst + 4 * j);
+                    o.x += prev.x;
+                    o.y += prev.y;
+                    o.z += prev.z;
+                    o.w += prev.w;
+                  }
+                  *reinterpret_cast<float4*>(dst + 4 * j) = o;
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) break;
+      if (EPI == EPI_LSE && row_ok) {
+        const long long o = (long long)s * ep.T + ep.row0 + r;
+        ep.pm[o] = run_max;
+        ep.ps[o] = run_sum;
+        ep.pd[o] = dot;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace kdkl

@@ -1,0 +1,206 @@
+"""ctypes binding of libkdkl.so (the C ABI in include/kdkl.h).
+
+Argument marshalling only: every step of the loss runs in the library's CUDA
+kernels. PyTorch provides device memory (outputs and the workspace) and the
+current stream. There is no CPU fallback: if the library is missing the calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkdkl.so")
+
+KD_OK = 0
+STATUS_NAMES = {
+    0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_SHAPE", 3: "KD_ERR_ALIGNMENT",
+    4: "KD_ERR_INDEX_RANGE", 5: "KD_ERR_WORKSPACE", 6: "KD_ERR_CUDA", 7: "KD_ERR_TIMEOUT",
+    8: "KD_ERR_UNSUPPORTED",
+}
+KDKL_MAX_K = 512
+
+
+class KDKLError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, STATUS_NAMES.get(code, "status %d" % code)))
+
+
+class kd_kl_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("K", ctypes.c_int32), ("temperature", ctypes.c_float), ("chunk", ctypes.c_int64)]
+
+
+class kd_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+# name -> (restype, argtypes); every symbol include/kdkl.h declares.
+_P = ctypes.c_void_p
+_SIGS = {
+    "kd_kl_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_kl_problem), ctypes.c_int]),
+    "kd_kl_forward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P, _P, _P,
+                                     _P, ctypes.c_size_t, _P]),
+    "kd_kl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P,
+                                      ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
+                                      _P]),
+    "kd_kl_check_status": (ctypes.c_int, [_P, _P]),
+    "kd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kd_launch_count": (ctypes.c_int64, []),
+    "kd_timing_begin": (ctypes.c_int, []),
+    "kd_timing_end": (ctypes.c_int, [ctypes.POINTER(kd_kernel_time), ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int)]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError("libkdkl.so not found at %s: build it with "
+                               "`python -m lm_head_top_gb300.build`" % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _problem(T, d, V, K, temperature, chunk) -> kd_kl_problem:
+    return kd_kl_problem(int(T), int(d), int(V), int(K), float(temperature), int(chunk))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be on a CUDA device" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def kd_status_string(code: int) -> str:
+    return load().kd_status_string(int(code)).decode()
+
+
+def kd_launch_count() -> int:
+    return int(load().kd_launch_count())
+
+
+def kd_kl_workspace_size(T, d, V, K, temperature=1.0, chunk=1024, which=0) -> int:
+    p = _problem(T, d, V, K, temperature, chunk)
+    return int(load().kd_kl_workspace_size(ctypes.byref(p), int(which)))
+
+
+def _workspace(p: kd_kl_problem, which: int, device, workspace):
+    need = int(load().kd_kl_workspace_size(ctypes.byref(p), which))
+    if need == 0:
+        raise KDKLError(2, "kd_kl_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def kd_kl_forward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0, chunk=1024,
+                  want_token_kl=False, loss=None, lse=None, token_kl=None, workspace=None,
+                  stream=None):
+    """Fused forward. Returns (loss [1] fp32, lse [T] fp32, token_kl [T] fp32 or None).
+    The work is queued on ``stream`` (default: torch's current stream)."""
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(topk_idx, "topk_idx", torch.int32, (T, K))
+    _check(topk_logit, "topk_logit", torch.float32, (T, K))
+    if mask is not None:
+        _check(mask, "mask", torch.uint8, (T,))
+    dev = H.device
+    p = _problem(T, d, V, K, temperature, chunk)
+    workspace = _workspace(p, 0, dev, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
+    if want_token_kl and token_kl is None:
+        token_kl = torch.empty(T, dtype=torch.float32, device=dev)
+    rc = load().kd_kl_forward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
+                              _ptr(mask), _ptr(loss), _ptr(lse), _ptr(token_kl), _ptr(workspace),
+                              workspace.numel(), _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_kl_forward")
+    return loss, lse, token_kl
+
+
+def kd_kl_backward(H, W, topk_idx, topk_logit, mask, lse, *, temperature=1.0, chunk=1024,
+                   grad_loss=1.0, dH=None, dW=None, accumulate_dW=False, workspace=None,
+                   stream=None):
+    """Fused backward of grad_loss * loss. Returns (dH [T,d] bf16, dW [V,d] fp32)."""
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(topk_idx, "topk_idx", torch.int32, (T, K))
+    _check(topk_logit, "topk_logit", torch.float32, (T, K))
+    _check(lse, "lse", torch.float32, (T,))
+    if mask is not None:
+        _check(mask, "mask", torch.uint8, (T,))
+    dev = H.device
+    p = _problem(T, d, V, K, temperature, chunk)
+    workspace = _workspace(p, 1, dev, workspace)
+    dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dH is None else dH
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    rc = load().kd_kl_backward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
+                               _ptr(mask), _ptr(lse), float(grad_loss), _ptr(dH), _ptr(dW),
+                               1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_kl_backward")
+    return dH, dW
+
+
+def kd_kl_check_status(workspace: torch.Tensor, stream=None) -> int:
+    """BLOCKING. Device-detected status of the latest call that used ``workspace``."""
+    return int(load().kd_kl_check_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def kd_timing_begin() -> None:
+    load().kd_timing_begin()
+
+
+def kd_timing_end(max_entries: int = 32):
+    """BLOCKING. Returns [(kernel name, launches, total ms)] since kd_timing_begin()."""
+    arr = (kd_kernel_time * max_entries)()
+    n = ctypes.c_int(0)
+    rc = load().kd_timing_end(arr, max_entries, ctypes.byref(n))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_timing_end")
+    return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, max_entries))]

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, rejects bad arguments before touching the device, and sizes a
+workspace that grows linearly in T with no T x V term."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lm_head_top_gb300 import kdkl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b(kd_[a-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kdkl.LIB_PATH):
+        from lm_head_top_gb300 import build
+        build.build()
+    return kdkl.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"kd_kl_forward", "kd_kl_backward", "kd_kl_workspace_size", "kd_kl_check_status",
+            "kd_status_string"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kdkl._SIGS) == names
+
+
+def test_status_strings(lib):
+    for code, name in kdkl.STATUS_NAMES.items():
+        assert kdkl.kd_status_string(code) == name
+
+
+def test_problem_struct_layout():
+    assert ctypes.sizeof(kdkl.kd_kl_problem) == 40
+    assert kdkl.kd_kl_problem.K.offset == 24 and kdkl.kd_kl_problem.chunk.offset == 32
+
+
+def _fwd(lib, p, H=16, W=16, idx=16, logit=16, ws=256, ws_bytes=1 << 30):
+    P = ctypes.c_void_p
+    return lib.kd_kl_forward(ctypes.byref(p), P(H), P(W), P(idx), P(logit), None, P(64), P(128),
+                             None, P(ws), ws_bytes, None)
+
+
+def _bwd(lib, p, **kw):
+    P = ctypes.c_void_p
+    return lib.kd_kl_backward(ctypes.byref(p), P(16), P(16), P(16), P(16), None, P(64), 1.0,
+                              P(kw.get("dH", 4096)), P(kw.get("dW", 8192)), 0, P(256), 1 << 30,
+                              None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d", 12, 3),            # d % 8 != 0 -> KD_ERR_ALIGNMENT
+    ("d", 0, 2),             # d < 8 -> KD_ERR_SHAPE
+    ("K", 0, 2),
+    ("K", 513, 2),           # > KDKL_MAX_K
+    ("K", 101, 2),           # K > V
+    ("T", -1, 2),
+    ("temperature", 0.0, 1),
+    ("temperature", float("inf"), 1),
+    ("chunk", 0, 1),
+])
+def test_argument_errors_are_synchronous(lib, field, value, code):
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 8)
+    setattr(p, field, value)
+    assert _fwd(lib, p) == code
+    assert _bwd(lib, p) == code
+    assert lib.kd_kl_workspace_size(ctypes.byref(p), 0) == 0
+
+
+def test_pointer_errors(lib):
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 8)
+    assert _fwd(lib, p, ws=0) == 5            # KD_ERR_WORKSPACE
+    assert _fwd(lib, p, H=0) == 1             # KD_ERR_INVALID_ARG
+    assert _fwd(lib, p, H=8) == 3             # H not 16-byte aligned
+    assert _fwd(lib, p, idx=2) == 3
+    assert _bwd(lib, p, dW=0) == 1
+    assert _bwd(lib, p, dH=24) == 3
+
+
+def test_valid_call_without_device_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 8)
+    assert _fwd(lib, p) in (6, 8)  # KD_ERR_CUDA or KD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["llama3b_8k", "gptoss20b_32k", "toyproj_256k"])
+def test_workspace_linear_in_T_no_TxV(lib, name):
+    from lm_head_top_gb300.inputs import WORKLOADS
+    w = WORKLOADS[name]
+    for which in (0, 1):
+        sizes = [kdkl.kd_kl_workspace_size(T, w.d, w.V, w.K, 1.0, w.chunk, which)
+                 for T in (w.T // 4, w.T // 2, w.T)]
+        assert all(s > 0 for s in sizes)
+        # a T x V term in bf16 would be at least 2*T*V bytes
+        assert sizes[-1] < 0.5 * 2 * w.T * w.V, (which, sizes)
+    # the gradient-of-logits buffer stays within chunk x V bf16 (+ tile padding)
+    bwd = kdkl.kd_kl_workspace_size(w.T, w.d, w.V, w.K, 1.0, w.chunk, 1)
+    per_token = 2 * 4 * w.K + 4 * w.d  # sorted teacher (id, p) + fp32 dH accumulator
+    g_budget = 2 * w.chunk * w.V * 1.07 + 2 * 256 * w.T + 2 * 128 * w.V
+    assert bwd <= w.T * per_token + g_budget + (1 << 20)

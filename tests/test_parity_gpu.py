@@ -1,0 +1,158 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element,
+on identical seeded inputs. Sizes here finish in the oracle within seconds and
+still span several 128 x 256 tiles, vocabulary slabs / token chunks and
+ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.kl_oracle as ok
+from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+from tests._helpers import GRAD_REL_L2, LOSS_RTOL, LSE_ATOL, rel_l2, run_gpu, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kdkl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_top_gb300 import kdkl as m
+    m.load()
+    return m
+
+
+def _compare(out, x, tau, grad_loss=1.0, dW_init=None):
+    H, W, idx, logit, mask = to_oracle(x)
+    r_loss, r_lse, r_kl = ok.forward(H, W, idx, logit, mask, tau)
+    r_dH, r_dW = ok.backward(H, W, idx, logit, mask, tau, grad_loss)
+    if dW_init is not None:
+        r_dW = r_dW + dW_init.numpy().astype(np.float64)
+    keep = mask != 0
+    errs = {
+        "loss": abs(out["loss"] - r_loss) / max(abs(r_loss), 1e-30),
+        "lse": float(np.abs(out["lse"] - r_lse).max()),
+        "kl": float(np.abs(out["token_kl"] - r_kl).max()),
+        "dH": rel_l2(out["dH"], r_dH),
+        "dW": rel_l2(out["dW"], r_dW),
+    }
+    assert errs["loss"] <= LOSS_RTOL, errs
+    assert errs["lse"] <= LSE_ATOL, errs
+    assert errs["kl"] <= 1e-3 * max(1.0, float(np.abs(r_kl).max())), errs
+    assert errs["dH"] <= GRAD_REL_L2, errs
+    assert errs["dW"] <= GRAD_REL_L2, errs
+    # masked rows of dH are exactly zero
+    assert not out["dH"][~keep].any()
+    return errs
+
+
+def test_small_workload(kdkl):
+    w = WORKLOADS["small"]
+    x = make_inputs(w, seed=0)
+    _compare(run_gpu(kdkl, x, w.tau, w.chunk), x, w.tau)
+
+
+@pytest.mark.parametrize("shape", [
+    # T, d, V, K, chunk, tau : ragged in every dimension, several vocabulary slabs
+    (131, 72, 1000, 7, 50, 2.0),
+    # more tokens than vocabulary: token chunks (dW accumulated across chunks)
+    (700, 64, 300, 5, 200, 1.0),
+    # one token, one teacher entry
+    (1, 8, 40, 1, 1, 1.0),
+    # K = V: the teacher covers the whole vocabulary
+    (64, 32, 48, 48, 16, 0.5),
+    # K = 512 (largest), V just above
+    (40, 48, 600, 512, 7, 1.0),
+])
+def test_ragged_shapes(kdkl, shape):
+    T, d, V, K, chunk, tau = shape
+    w = WORKLOADS["small"].with_(T=T, d=d, V=V, K=K, chunk=chunk, tau=tau,
+                                 seq_len=max(T // 3, 1), pad_frac=0.25)
+    x = make_inputs(w, seed=1)
+    if x["mask"].sum() == 0:
+        x["mask"][0] = 1
+    _compare(run_gpu(kdkl, x, tau, chunk, grad_loss=0.75), x, tau, grad_loss=0.75)
+
+
+def test_accumulate_dW(kdkl):
+    w = WORKLOADS["small"].with_(T=300, d=64, V=2000, K=9, chunk=100)
+    x = make_inputs(w, seed=2)
+    dW0 = torch.randn(2000, 64, dtype=torch.float32) * 1e-3
+    _compare(run_gpu(kdkl, x, w.tau, w.chunk, dW_init=dW0), x, w.tau, dW_init=dW0)
+
+
+def test_half_overlap_teacher(kdkl):
+    w = WORKLOADS["small"].with_(T=384, d=128, V=3000, K=20, chunk=128, teacher="half_overlap")
+    x = make_inputs(w, seed=3, topk_device="cpu")
+    _compare(run_gpu(kdkl, x, w.tau, w.chunk), x, w.tau)
+
+
+def test_chunk_invariance(kdkl):
+    w = WORKLOADS["small"].with_(T=256, d=64, V=2500, K=10)
+    x = make_inputs(w, seed=4)
+    outs = [run_gpu(kdkl, x, 1.0, c) for c in (1, 37, 256, 100000)]
+    for o in outs[1:]:
+        assert o["loss"] == outs[0]["loss"]  # the forward does not depend on chunk
+        assert rel_l2(o["dH"], outs[0]["dH"]) < 1e-2
+        assert rel_l2(o["dW"], outs[0]["dW"]) < 1e-5
+
+
+def test_all_masked(kdkl):
+    w = WORKLOADS["small"].with_(T=130, d=32, V=700, K=4, chunk=64)
+    x = make_inputs(w, seed=5)
+    x["mask"].zero_()
+    out = run_gpu(kdkl, x, 1.0, 64)
+    assert out["loss"] == 0.0
+    assert not out["dH"].any() and not out["dW"].any()
+
+
+def test_no_mask_pointer_means_all_tokens(kdkl):
+    w = WORKLOADS["small"].with_(T=200, d=40, V=900, K=6, chunk=64)
+    x = make_inputs(w, seed=6)
+    a = run_gpu(kdkl, x, 1.0, 64, mask=False)
+    b = run_gpu(kdkl, x, 1.0, 64, mask=True)
+    assert a["loss"] == b["loss"]
+    assert rel_l2(a["dW"], b["dW"]) < 1e-6
+
+
+def test_zero_tokens(kdkl):
+    dev = "cuda:0"
+    H = torch.empty(0, 16, dtype=torch.bfloat16, device=dev)
+    W = torch.randn(50, 16, device=dev).to(torch.bfloat16)
+    idx = torch.empty(0, 3, dtype=torch.int32, device=dev)
+    lg = torch.empty(0, 3, dtype=torch.float32, device=dev)
+    loss, lse, _ = kdkl.kd_kl_forward(H, W, idx, lg, None, temperature=1.0, chunk=8)
+    dH, dW = kdkl.kd_kl_backward(H, W, idx, lg, None, lse, temperature=1.0, chunk=8)
+    torch.cuda.synchronize()
+    assert loss.item() == 0.0 and dW.abs().max().item() == 0.0
+
+
+def test_device_detected_index_error(kdkl):
+    w = WORKLOADS["small"].with_(T=64, d=16, V=100, K=3, chunk=16)
+    x = make_inputs(w, seed=7)
+    x["topk_idx"][5, 1] = 100  # == V: out of range
+    g = {k: v.cuda() for k, v in x.items()}
+    ws = torch.empty(kdkl.kd_kl_workspace_size(64, 16, 100, 3, 1.0, 16, 0), dtype=torch.uint8,
+                     device="cuda")
+    kdkl.kd_kl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], chunk=16,
+                       workspace=ws)
+    assert kdkl.kd_kl_check_status(ws) == 4  # KD_ERR_INDEX_RANGE
+    x["topk_idx"][5, 1] = 3
+    g = {k: v.cuda() for k, v in x.items()}
+    kdkl.kd_kl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], chunk=16,
+                       workspace=ws)
+    assert kdkl.kd_kl_check_status(ws) == 0
+
+
+def test_timing_and_launch_count(kdkl):
+    w = WORKLOADS["small"].with_(T=128, d=64, V=1024, K=8, chunk=64)
+    x = make_inputs(w, seed=8)
+    before = kdkl.kd_launch_count()
+    kdkl.kd_timing_begin()
+    run_gpu(kdkl, x, 1.0, 64)
+    rows = kdkl.kd_timing_end()
+    names = {r[0] for r in rows}
+    assert {"teacher_prep", "fwd_lse_gemm", "lse_combine", "loss_finalize", "bwd_grad_gemm",
+            "dH_gemm", "dW_gemm", "f32_to_bf16"} <= names
+    assert kdkl.kd_launch_count() - before == sum(r[1] for r in rows)
+    assert all(r[2] > 0 for r in rows)

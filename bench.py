@@ -1,0 +1,384 @@
+"""Benchmark of the fused chunked KL distillation loss (forward + backward).
+
+One step = kd_kl_forward + kd_kl_backward over one batch of synthetic input:
+the GPT-OSS-20B-like student head at 32,768 tokens (d = 2880, V = 201,088,
+K = 100 teacher entries, chunk = 2048, tau = 1). Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {kdkl,reference}]
+
+With N > 1 it is launched by torch.distributed.run, one rank per GPU; every
+rank runs its own batch (weak scaling, no data-path collective) and rank 0
+reports the max time over ranks. ``--impl reference`` times the fp64 CPU
+oracle on bounded token samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fused chunked KL fwd+bwd tokens/s, % of BF16 tensor peak, peak HBM GiB"
+WORKLOAD = "gptoss20b_32k"
+SPEC_BF16_TFLOPS = 2250.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_KERNELS = ("fwd_lse_gemm", "bwd_grad_gemm", "dH_gemm", "dW_gemm")
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "lm_head_top_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        with open(os.path.join(cdir, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    summary was taken on the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("csrc_sha256_16") != csrc_digest() or d.get("workload") != WORKLOAD:
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else float(k["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        return False
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        finally:
+            os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# --------------------------------------------------------------- oracle timing
+
+def oracle_sample_step(x_np, w, rows):
+    """fp64 oracle forward + backward on a sample of token rows (all V, all d)."""
+    import oracle.kl_oracle as ok
+    H, W, idx, logit, mask = x_np
+    Hs, idxs, lgs, ms = H[rows], idx[rows], logit[rows], mask[rows]
+    ok.forward(Hs, W, idxs, lgs, ms, w.tau)
+    ok.backward(Hs, W, idxs, lgs, ms, w.tau, 1.0)
+
+
+def oracle_arrays(x):
+    import oracle.kl_oracle as ok
+    return (ok.bf16_bits_to_f64(x["H"].view(torch.int16).numpy()),
+            ok.bf16_bits_to_f64(x["W"].view(torch.int16).numpy()),
+            x["topk_idx"].numpy().astype(np.int64), x["topk_logit"].numpy().astype(np.float64),
+            x["mask"].numpy())
+
+
+def time_oracle(x_np, w, n_tokens: int, repeats: int = 1):
+    rng = np.random.default_rng(0)
+    times = []
+    for _ in range(repeats):
+        rows = np.sort(rng.choice(w.T, size=n_tokens, replace=False))
+        t0 = time.perf_counter()
+        oracle_sample_step(x_np, w, rows)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+# ------------------------------------------------------------------- main arm
+
+def run_kdkl(args):
+    from lm_head_top_gb300 import kdkl
+    from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    kdkl.load()
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, seed=rank, topk_device=dev)
+    T, d, V, K = w.T, w.d, w.V, w.K
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    g = {k: v.to(dev) for k, v in x.items()}
+    ws_f = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 0), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 1), dtype=torch.uint8,
+                       device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dH = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(gg):
+        kdkl.kd_kl_forward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"],
+                           temperature=w.tau, chunk=w.chunk, loss=loss, lse=lse, workspace=ws_f,
+                           stream=stream)
+        kdkl.kd_kl_backward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"], lse,
+                            temperature=w.tau, chunk=w.chunk, grad_loss=1.0, dH=dH, dW=dW,
+                            workspace=ws_b, stream=stream)
+
+    for _ in range(args.warmup):
+        step(g)
+    torch.cuda.synchronize(dev)
+    st = kdkl.kd_kl_check_status(ws_f)
+    st_b = kdkl.kd_kl_check_status(ws_b)
+    if st or st_b:
+        raise SystemExit("device status after warm-up: %s / %s" % (kdkl.kd_status_string(st),
+                                                                   kdkl.kd_status_string(st_b)))
+
+    # ---- device-resident timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kdkl.kd_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        kdkl.kd_timing_begin()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(g)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_kernel = kdkl.kd_timing_end()
+        barrier(world)
+    launches = kdkl.kd_launch_count() - launches0
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    clk = clocks.summary()
+    peak_hbm = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+
+    # ---- end to end: pinned host inputs copied in, loss read back, every step
+    host = {k: v.pin_memory() for k, v in x.items() if k != "W"}
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    gin = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for k in gin:
+            gin[k].copy_(host[k], non_blocking=True)
+        step(gin)
+        loss_host.copy_(loss, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    result = None
+    if rank == 0:
+        pk, pk_src = peaks()
+        tokens = T * world * args.steps
+        flops_step = 8.0 * T * V * d  # 4 GEMM-equivalents per step and GPU
+        tflops = flops_step * args.steps / (elapsed_ms / 1e3) / 1e12
+        # dominant kernel by device time; algorithmic flops per launch = 2 T V d
+        # per step for each of the four GEMM kinds, split over its launches
+        rows = {n: (c, ms) for n, c, ms in per_kernel}
+        dom = max(rows, key=lambda n: rows[n][1])
+        dom_launches, dom_ms = rows[dom]
+        if dom in GEMM_KERNELS:
+            per_launch_flops = 2.0 * T * V * d * args.steps / dom_launches
+            achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
+            peak = pk["bf16_tflops_sustained"]
+            roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_source": "%s bf16_tflops_sustained" % pk_src,
+                    "flops_per_launch": per_launch_flops,
+                    "avg_launch_ms": round(dom_ms / dom_launches, 4),
+                    "traffic": recorded_traffic(dom)}
+        else:
+            roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": None, "traffic": recorded_traffic(dom)}
+        # CPU baseline: the fp64 oracle on a bounded token sample, this host
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            x_np = oracle_arrays(x)
+            n_cpu = args.cpu_tokens
+            t = time_oracle(x_np, w, n_cpu)[0]
+            cpu = {"value": round(n_cpu / t, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                   "kind": "oracle",
+                   "sample": "fp64 oracle forward+backward on %d random tokens of %s (all V=%d, "
+                             "d=%d; dense logits row block), %.1f s" % (n_cpu, WORKLOAD, V, d, t)}
+        result = {
+            "metric": METRIC,
+            "value": round(tokens / (elapsed_ms / 1e3), 1),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 3),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; bf16 H~N(0,1), W~N(0,1/d); teacher top-100 half from "
+                    "the student's own top-100)",
+            "config": {"workload": WORKLOAD, "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
+                       "tau": w.tau, "global_batch_tokens": T * world,
+                       "parallelism": "dp%d (independent batches)" % world,
+                       "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
+            "tflops": round(tflops, 1),
+            "pct_bf16_spec_peak": round(100 * tflops / SPEC_BF16_TFLOPS, 2),
+            "pct_bf16_measured_sustained": round(100 * tflops / pk["bf16_tflops_sustained"], 2),
+            "peak_hbm_gib": round(peak_hbm, 3),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+            "gpu_launches": launches,
+            "kernel_ms_per_step": {n: round(ms / args.steps, 3) for n, c, ms in per_kernel},
+            "clocks": clk,
+        }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_reference(args):
+    """The fp64 CPU oracle on bounded token samples of the same workload."""
+    from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, seed=0)
+    x_np = oracle_arrays(x)
+    n = args.ref_tokens
+    for _ in range(args.warmup):
+        time_oracle(x_np, w, n)
+    times = time_oracle(x_np, w, n, repeats=args.steps)
+    total = sum(times)
+    value = n * args.steps / total
+    cpu = {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": "fp64 oracle forward+backward on %d random tokens of %s per step "
+                     "(all V=%d, d=%d)" % (n, WORKLOAD, w.V, w.d)}
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
+                   "tau": w.tau, "sample_tokens_per_step": n},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("kdkl", "reference"), default="kdkl")
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "kdkl":
+        args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
+    res = run_reference(args) if args.impl == "reference" else run_kdkl(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

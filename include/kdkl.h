@@ -105,6 +105,32 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
                          uint16_t* dH, float* dW, int accumulate_dW,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free forward. The paper has no counterpart to this call; it
+ * exists for callers that cannot allocate device memory for a workspace: code
+ * inside a host framework whose memory pool owns (and has typically reserved)
+ * all free HBM, and loops with a latency budget that rules out cudaMalloc,
+ * which can synchronise the device.
+ * Same arguments, results and errors as kd_kl_forward, minus the workspace:
+ * the scratch is a fixed array of KDKL_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, held on every GPU where the library's device code is loaded until
+ * the process exits. Problems whose kd_kl_workspace_size(prob, 0) exceeds it
+ * return KD_ERR_WORKSPACE before anything is queued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine (with
+ *     per-kernel timing off, the default).
+ *   - Every call on a device shares the one array and clears its header when
+ *     it starts. Calls whose GPU work overlaps (other streams, other host
+ *     threads) race on it: order them on one stream.
+ *   - Device-detected errors of these calls cannot be read back with
+ *     kd_kl_check_status (there is no workspace pointer to pass). */
+#define KDKL_NOALLOC_SCRATCH_BYTES (64u << 20)
+kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                                const int32_t* topk_idx, const float* topk_logit,
+                                const uint8_t* mask, float* loss, float* lse, float* token_kl,
+                                void* stream);
+
 /* BLOCKING: synchronises `stream`, then returns the first device-detected
  * error recorded in `workspace` by the latest call that used it (KD_OK if
  * none). Each forward/backward call clears the record when it starts. */

@@ -50,6 +50,8 @@ _SIGS = {
     "kd_kl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P,
                                       ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
                                       _P]),
+    "kd_kl_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _P]),
     "kd_kl_check_status": (ctypes.c_int, [_P, _P]),
     "kd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kd_launch_count": (ctypes.c_int64, []),
@@ -184,6 +186,35 @@ def kd_kl_backward(H, W, topk_idx, topk_logit, mask, lse, *, temperature=1.0, ch
     if rc != KD_OK:
         raise KDKLError(rc, "kd_kl_backward")
     return dH, dW
+
+
+def kd_kl_forward_noalloc(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0,
+                          chunk=1024, want_token_kl=False, loss=None, lse=None, token_kl=None,
+                          stream=None):
+    """Forward for callers that cannot allocate a workspace: the library's own
+    fixed scratch array is used instead (see kd_kl_forward_noalloc in kdkl.h).
+    Outputs are allocated here only when not passed in."""
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(topk_idx, "topk_idx", torch.int32, (T, K))
+    _check(topk_logit, "topk_logit", torch.float32, (T, K))
+    if mask is not None:
+        _check(mask, "mask", torch.uint8, (T,))
+    dev = H.device
+    p = _problem(T, d, V, K, temperature, chunk)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
+    if want_token_kl and token_kl is None:
+        token_kl = torch.empty(T, dtype=torch.float32, device=dev)
+    rc = load().kd_kl_forward_noalloc(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
+                                      _ptr(topk_logit), _ptr(mask), _ptr(loss), _ptr(lse),
+                                      _ptr(token_kl), _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_kl_forward_noalloc")
+    return loss, lse, token_kl
 
 
 def kd_kl_check_status(workspace: torch.Tensor, stream=None) -> int:

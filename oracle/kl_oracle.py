@@ -157,6 +157,33 @@ def lse_rows(H, W, tau: float, rows_per_block: int = 256) -> np.ndarray:
     return out
 
 
+def forward_all_rows(H, W, topk_idx, topk_logit, tau: float, rows_per_block: int = 128,
+                     workers: int | None = None):
+    """(lse [T], token_kl [T]) for every row: ``forward`` applied to blocks of
+    rows, the blocks run by a thread pool (numpy releases the GIL in BLAS and
+    in the elementwise steps). Each row's arithmetic is exactly ``forward``'s."""
+    import concurrent.futures as cf
+    import os
+
+    H = np.asarray(H)
+    W = np.asarray(W, dtype=np.float64)
+    T = H.shape[0]
+    lse = np.empty(T, dtype=np.float64)
+    kl = np.empty(T, dtype=np.float64)
+    ones = np.ones(T, dtype=np.uint8)
+
+    def block(r0):
+        r1 = min(r0 + rows_per_block, T)
+        _, l, k = forward(H[r0:r1], W, topk_idx[r0:r1], topk_logit[r0:r1], ones[r0:r1], tau)
+        lse[r0:r1] = l
+        kl[r0:r1] = k
+
+    n = workers or max(1, min(8, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(n) as ex:
+        list(ex.map(block, range(0, T, rows_per_block)))
+    return lse, kl
+
+
 def dW_rows(H, W, topk_idx, topk_logit, mask, tau: float, vocab_rows, lse,
             grad_loss: float = 1.0) -> np.ndarray:
     """dW[v, :] = sum_t G_{t,v} H_t for the listed vocabulary rows v, given the

@@ -371,3 +371,12 @@ def test_planted_transposed_backward_is_caught(monkeypatch):
     assert not _pins_pass(ok)
     monkeypatch.setattr(ok, "backward", real)
     assert _pins_pass(ok)
+
+
+def test_forward_all_rows_matches_forward():
+    rng = np.random.default_rng(15)
+    H, W, idx, logit, mask = _rand_problem(rng, 50, 8, 60, 5, mask_p=1.0)
+    _, lse, kl = ok.forward(H, W, idx, logit, mask, 1.3)
+    lse2, kl2 = ok.forward_all_rows(H, W, idx, logit, 1.3, rows_per_block=7, workers=3)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-14)
+    np.testing.assert_allclose(kl2, kl, rtol=1e-12, atol=1e-14)

@@ -191,7 +191,9 @@ def run_kdkl(args):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     kdkl.load()
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_(T=args.tokens)
     x = make_inputs(w, seed=rank, topk_device=dev)
     T, d, V, K = w.T, w.d, w.V, w.K
 
@@ -244,23 +246,25 @@ def run_kdkl(args):
     peak_hbm = torch.cuda.max_memory_allocated(dev) / 2 ** 30
 
     # ---- end to end: pinned host inputs copied in, loss read back, every step
-    host = {k: v.pin_memory() for k, v in x.items() if k != "W"}
-    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    gin = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(args.steps):
-        for k in gin:
-            gin[k].copy_(host[k], non_blocking=True)
-        step(gin)
-        loss_host.copy_(loss, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_ms, h2d = None, 0
+    if not args.no_e2e:
+        host = {k: v.pin_memory() for k, v in x.items() if k != "W"}
+        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        gin = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for k in gin:
+                gin[k].copy_(host[k], non_blocking=True)
+            step(gin)
+            loss_host.copy_(loss, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     result = None
     if rank == 0:
@@ -310,7 +314,7 @@ def run_kdkl(args):
             "dtype": "bf16",
             "data": "synthetic (seeded; bf16 H~N(0,1), W~N(0,1/d); teacher top-100 half from "
                     "the student's own top-100)",
-            "config": {"workload": WORKLOAD, "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
+            "config": {"workload": w.name if not args.tokens else "%s_T%d" % (w.name, T), "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
                        "tau": w.tau, "global_batch_tokens": T * world,
                        "parallelism": "dp%d (independent batches)" % world,
                        "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
@@ -320,8 +324,9 @@ def run_kdkl(args):
             "peak_hbm_gib": round(peak_hbm, 3),
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+            "e2e": None if e2e_ms is None else {
+                "value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
             "gpu_launches": launches,
             "kernel_ms_per_step": {n: round(ms / args.steps, 3) for n, c, ms in per_kernel},
             "clocks": clk,
@@ -369,9 +374,13 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("kdkl", "reference"), default="kdkl")
-    ap.add_argument("--cpu-tokens", type=int, default=256)
-    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="another workload's shapes, for profiling small cases")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     args = ap.parse_args()
     if args.impl == "kdkl":
         args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps

@@ -147,13 +147,26 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Vocabulary splits per 128-row tile so that (row tiles x splits) units share
-// out evenly over the persistent CTAs: minimises waves x tiles per unit.
-int choose_nsplit(int m_tiles, int n_tiles, int num_sms) {
-  int best = 1;
+// Split plan for the logit GEMMs (forward and backward recompute): how many
+// vocabulary splits per 128-row tile, and how many splits form one L2 group.
+// A group keeps G_m = num_sms / group_n m-tiles in flight; their A rows
+// (128 x d bf16 each) must stay resident in L2 while the group's B tiles
+// stream past, so G_m is capped by kL2RowBudget. Among split counts that are
+// multiples of group_n, pick the one with the least waves x tiles per unit.
+struct SplitPlan {
+  int nsplit, group_n;
+};
+constexpr double kL2RowBudget = 24.0 * 1024 * 1024;
+
+SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d) {
+  const double a_tile_bytes = (double)BM * (double)d * 2.0;
+  int gm = (int)std::max(1.0, std::floor(kL2RowBudget / a_tile_bytes));
+  gm = std::min(gm, m_tiles);
+  int group_n = (num_sms + gm - 1) / gm;
+  group_n = std::max(1, std::min(group_n, n_tiles));
+  SplitPlan best{group_n, group_n};
   double best_cost = 1e300;
-  const int cap = std::min(n_tiles, 4096);
-  for (int ns = 1; ns <= cap; ++ns) {
+  for (int ns = group_n; ns <= n_tiles; ns += group_n) {
     const int64_t units = (int64_t)m_tiles * ns;
     const int64_t grid = std::min<int64_t>(units, num_sms);
     const int64_t waves = ceil_div(units, grid);
@@ -161,14 +174,14 @@ int choose_nsplit(int m_tiles, int n_tiles, int num_sms) {
     const double cost = (double)waves * ((double)per_unit + 0.05);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
-      best = ns;
+      best.nsplit = ns;
     }
   }
   return best;
 }
 
 struct FwdPlan {
-  int m_tiles, n_tiles, nsplit, grid;
+  int m_tiles, n_tiles, nsplit, group_n, grid;
   size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_bsum, total;
 };
 
@@ -195,7 +208,9 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms) {
   FwdPlan f{};
   f.m_tiles = (int)ceil_div(p.T, BM);
   f.n_tiles = (int)ceil_div(p.V, BN);
-  f.nsplit = p.T > 0 ? choose_nsplit(f.m_tiles, f.n_tiles, num_sms) : 1;
+  const SplitPlan sp = choose_split(std::max(f.m_tiles, 1), f.n_tiles, num_sms, p.d);
+  f.nsplit = p.T > 0 ? sp.nsplit : 1;
+  f.group_n = p.T > 0 ? sp.group_n : 1;
   f.grid = (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, num_sms);
   size_t o = kHeaderBytes;
   const size_t TK = (size_t)p.T * p.K;
@@ -351,6 +366,7 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   sh.m_tiles = f.m_tiles;
   sh.n_tiles = f.n_tiles;
   sh.nsplit = f.nsplit;
+  sh.group_n = f.group_n;
   sh.units = f.m_tiles * f.nsplit;
   sh.k_blocks = (int)ceil_div(d, BK);
   EpiParams ep{};
@@ -430,7 +446,9 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         GemmShape sh{};
         sh.m_tiles = (int)ceil_div(rows, BM);
         sh.n_tiles = (int)ceil_div(cols, BN);
-        sh.nsplit = choose_nsplit(sh.m_tiles, sh.n_tiles, di.num_sms);
+        const SplitPlan spl = choose_split(sh.m_tiles, sh.n_tiles, di.num_sms, d);
+        sh.nsplit = spl.nsplit;
+        sh.group_n = spl.group_n;
         sh.units = sh.m_tiles * sh.nsplit;
         sh.k_blocks = (int)ceil_div(d, BK);
         sh.a_m0 = row0;
@@ -462,6 +480,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         sh.m_tiles = (int)ceil_div(rows, BM);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
+        sh.group_n = dn_tiles;
         sh.units = sh.m_tiles * sh.nsplit;
         sh.k_blocks = (int)ceil_div(cols, BK);
         sh.b_k0 = col0;
@@ -482,6 +501,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         sh.m_tiles = (int)ceil_div(cols, BM);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
+        sh.group_n = dn_tiles;
         sh.units = sh.m_tiles * sh.nsplit;
         sh.k_blocks = (int)ceil_div(rows, BK);
         sh.b_k0 = row0;

@@ -45,10 +45,16 @@ constexpr uint32_t MN_ATOM_BYTES = BK * 128;
 
 enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2 };
 
-// Work decomposition: `units` = m_tiles * nsplit; unit u covers m-tile u / nsplit
-// and a contiguous range of n-tiles (split u % nsplit of n_tiles).
+// Work decomposition: `units` = m_tiles * nsplit. A unit is one m-tile and one
+// split (a contiguous range of n-tiles). Units are numbered group by group:
+// the splits form groups of `group_n`; inside a group the split index runs
+// fastest, then the m-tile. Consecutive units (the ones in flight together on
+// the persistent CTAs) therefore cover ~num_CTAs/group_n m-tiles x group_n
+// splits: the A rows of those m-tiles stay in L2 while every B tile is fetched
+// from DRAM once per pass of such a group. group_n == nsplit gives plain
+// m-major order.
 struct GemmShape {
-  int m_tiles, n_tiles, nsplit, units;
+  int m_tiles, n_tiles, nsplit, group_n, units;
   int k_blocks;
   int a_m0, a_k0;  // A coordinate offsets (rows M / reduction K)
   int b_n0, b_k0;  // B coordinate offsets (rows N / reduction K)
@@ -85,8 +91,12 @@ struct EpiParams {
 
 __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
                                             int& ne) {
-  m = u / sh.nsplit;
-  s = u - m * sh.nsplit;
+  const int per_group = sh.m_tiles * sh.group_n;
+  const int g = u / per_group;
+  const int r = u - g * per_group;
+  const int gsize = min(sh.group_n, sh.nsplit - g * sh.group_n);  // last group may be short
+  m = r / gsize;
+  s = g * sh.group_n + (r - m * gsize);
   nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
   ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
 }

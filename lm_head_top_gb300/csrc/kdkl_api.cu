@@ -20,6 +20,7 @@
 // dH [T,d]. Both tilings give the same sums.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -259,6 +260,14 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Failure-detection test hook: with KDKL_INJECT_STALL=1 in the environment the
+// GEMM kernels stall on purpose, their bounded waits run out after 2 ms and
+// the call reports KD_ERR_TIMEOUT through kd_kl_check_status. Read per call.
+int inject_stall_from_env() {
+  const char* v = getenv("KDKL_INJECT_STALL");
+  return (v && v[0] == '1') ? 1 : 0;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -363,6 +372,7 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW, W, d, V, d, BK, BN))
     return KD_ERR_CUDA;
   GemmShape sh{};
+  sh.inject_stall = inject_stall_from_env();
   sh.m_tiles = f.m_tiles;
   sh.n_tiles = f.n_tiles;
   sh.nsplit = f.nsplit;
@@ -433,6 +443,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
     return KD_ERR_CUDA;
 
   const int dn_tiles = (int)ceil_div(d, BN);
+  const int stall = inject_stall_from_env();
   for (int64_t tb = 0; tb < b.n_tblocks; ++tb) {
     const int row0 = (int)(tb * b.Tb);
     const int rows = (int)std::min<int64_t>(b.Tb, p.T - row0);
@@ -444,6 +455,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
       // 1) recompute the logits of the block and store (softmax - P) * m g / (tau N)
       {
         GemmShape sh{};
+        sh.inject_stall = stall;
         sh.m_tiles = (int)ceil_div(rows, BM);
         sh.n_tiles = (int)ceil_div(cols, BN);
         const SplitPlan spl = choose_split(sh.m_tiles, sh.n_tiles, di.num_sms, d);
@@ -477,6 +489,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         CUtensorMap tmG_K;
         if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM)) return KD_ERR_CUDA;
         GemmShape sh{};
+        sh.inject_stall = stall;
         sh.m_tiles = (int)ceil_div(rows, BM);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
@@ -498,6 +511,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         CUtensorMap tmG_MN;
         if (!encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK)) return KD_ERR_CUDA;
         GemmShape sh{};
+        sh.inject_stall = stall;
         sh.m_tiles = (int)ceil_div(cols, BM);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;

@@ -58,6 +58,10 @@ struct GemmShape {
   int k_blocks;
   int a_m0, a_k0;  // A coordinate offsets (rows M / reduction K)
   int b_n0, b_k0;  // B coordinate offsets (rows N / reduction K)
+  // Failure-detection test only: the producer issues nothing, so the MMA
+  // warp's first wait runs out (after kInjectedWaitLimitNs) and the block
+  // unwinds through its error path. Never set in normal calls.
+  int inject_stall;
 };
 
 struct EpiParams {
@@ -133,6 +137,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t limit = sh.inject_stall ? kInjectedWaitLimitNs : kWaitLimitNs;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -165,13 +170,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long fills = 0;
-      bool ok = true;
+      bool ok = sh.inject_stall == 0;
       for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
           for (int kb = 0; kb < sh.k_blocks; ++kb) {
-            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status, limit)) {
               ok = false;
               break;
             }
@@ -221,14 +226,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
-          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) {
+          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, limit)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           for (int kb = 0; kb < sh.k_blocks; ++kb) {
-            if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status)) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status, limit)) {
               ok = false;
               break;
             }
@@ -295,7 +300,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       for (int n = nb; n < ne; ++n) {
-        bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status);
+        bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status, limit);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
           ok = false;

@@ -21,6 +21,8 @@ enum : int {
 // A pipeline wait that has not completed after this long (globaltimer ns)
 // records DEV_ERR_TIMEOUT and lets the kernel unwind instead of spinning.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+// Shorter limit used when a stall is injected on purpose (failure-detection test).
+constexpr uint64_t kInjectedWaitLimitNs = 2000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -71,14 +73,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // the block's abort flag plus the device status) if the wait runs out, or if
 // another role of the block has already aborted.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort_flag, int* status) {
+                                                  volatile int* abort_flag, int* status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         record_error(status, DEV_ERR_TIMEOUT);
         return false;

@@ -149,9 +149,10 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Split plan for the logit GEMMs (forward and backward recompute): how many
-// vocabulary splits per 128-row tile, and how many splits form one L2 group.
-// A group keeps G_m = num_sms / group_n m-tiles in flight; their A rows
-// (128 x d bf16 each) must stay resident in L2 while the group's B tiles
+// vocabulary splits per m-tile, and how many splits form one L2 group.
+// `num_sms` here counts unit processors (CTAs, or CTA pairs). A group keeps
+// G_m = num_sms / group_n m-tiles in flight; their A rows (tile_m x d bf16
+// each) must stay resident in L2 while the group's B tiles
 // stream past, so G_m is capped by kL2RowBudget. Among split counts that are
 // multiples of group_n, pick the one with the least waves x tiles per unit.
 struct SplitPlan {
@@ -159,8 +160,8 @@ struct SplitPlan {
 };
 constexpr double kL2RowBudget = 24.0 * 1024 * 1024;
 
-SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d) {
-  const double a_tile_bytes = (double)BM * (double)d * 2.0;
+SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d, int tile_m) {
+  const double a_tile_bytes = (double)tile_m * (double)d * 2.0;
   int gm = (int)std::max(1.0, std::floor(kL2RowBudget / a_tile_bytes));
   gm = std::min(gm, m_tiles);
   int group_n = (num_sms + gm - 1) / gm;
@@ -182,6 +183,7 @@ SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d) {
 }
 
 struct FwdPlan {
+  bool pair;
   int m_tiles, n_tiles, nsplit, group_n, grid;
   size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_bsum, total;
 };
@@ -205,14 +207,16 @@ bool problem_ok(const kd_kl_problem* p) {
   return true;
 }
 
-FwdPlan plan_forward(const kd_kl_problem& p, int num_sms) {
+FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs) {
   FwdPlan f{};
-  f.m_tiles = (int)ceil_div(p.T, BM);
-  f.n_tiles = (int)ceil_div(p.V, BN);
-  const SplitPlan sp = choose_split(std::max(f.m_tiles, 1), f.n_tiles, num_sms, p.d);
+  const int tile_m = pair ? 2 * BM : BM;
+  f.pair = pair;
+  f.m_tiles = (int)ceil_div(p.T, tile_m);
+  f.n_tiles = (int)ceil_div(p.V, LOGIT_BN);
+  const SplitPlan sp = choose_split(std::max(f.m_tiles, 1), f.n_tiles, procs, p.d, tile_m);
   f.nsplit = p.T > 0 ? sp.nsplit : 1;
   f.group_n = p.T > 0 ? sp.group_n : 1;
-  f.grid = (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, num_sms);
+  f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
   size_t o = kHeaderBytes;
   const size_t TK = (size_t)p.T * p.K;
   f.off_sidx = o; o = align256(o + TK * 4);
@@ -247,7 +251,7 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
     b.n_vblocks = 1;
   }
   b.Tb_pad = round_up(b.Tb, BM);
-  b.Vb_pad = round_up(b.Vb, BN);
+  b.Vb_pad = round_up(b.Vb, LOGIT_BN);
   size_t o = kHeaderBytes;
   const size_t TK = (size_t)p.T * p.K;
   b.off_sidx = o; o = align256(o + TK * 4);
@@ -259,6 +263,36 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
 }
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// GEMM tiling mode: 2-CTA pairs (cta_group::2, 256-row tiles, half the B
+// bytes per CTA) unless KDKL_CTA_PAIR=0 selects single-CTA 128-row tiles.
+// Both compute the same sums; the switch exists to compare them.
+bool use_pair() {
+  const char* v = getenv("KDKL_CTA_PAIR");
+  return !(v && v[0] == '0');
+}
+
+// KDKL_LOG_PLAN=1 prints each GEMM launch plan to stderr (tuning aid).
+bool log_plan() {
+  const char* v = getenv("KDKL_LOG_PLAN");
+  return v && v[0] == '1';
+}
+
+void print_plan(const char* what, bool pair, int procs, const GemmShape& sh, int grid) {
+  fprintf(stderr,
+          "[kdkl] %s pair=%d procs=%d max_clusters=%d m_tiles=%d n_tiles=%d nsplit=%d "
+          "group_n=%d units=%d k_blocks=%d grid=%d\n",
+          what, pair ? 1 : 0, procs, pair ? pair_max_active_clusters() : 0, sh.m_tiles,
+          sh.n_tiles, sh.nsplit, sh.group_n, sh.units, sh.k_blocks, grid);
+}
+
+// Unit processors of the persistent GEMM grid: CTAs, or co-resident CTA pairs.
+int gemm_procs(int num_sms, bool pair) {
+  if (!pair) return num_sms;
+  const int fit = pair_max_active_clusters();
+  const int half = num_sms / 2;
+  return std::max(1, fit > 0 ? std::min(half, fit) : half);
+}
 
 // Failure-detection test hook: with KDKL_INJECT_STALL=1 in the environment the
 // GEMM kernels stall on purpose, their bounded waits run out after 2 ms and
@@ -309,9 +343,13 @@ size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which) {
   if (which == 0) {
     DeviceInfo di;
     const int sms = (device_info(&di) == KD_OK) ? di.num_sms : 148;
-    // The split count depends on the SM count; size for the larger of the
-    // device's plan and a 1-split plan so the answer is safe either way.
-    return std::max(plan_forward(*prob, sms).total, plan_forward(*prob, 1).total);
+    // The split count depends on the SM count and the tiling mode; size for
+    // the larger of the two modes so the answer holds for either.
+    // Pair plans are sized for any number of co-resident clusters up to sms/2.
+    size_t total = plan_forward(*prob, sms, false, sms).total;
+    for (int procs = 1; procs <= sms / 2; ++procs)
+      total = std::max(total, plan_forward(*prob, sms, true, procs).total);
+    return total;
   }
   if (which == 1) return plan_backward(*prob).total;
   return 0;
@@ -347,7 +385,8 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   if ((st = device_info(&di)) != KD_OK) return st;
   if ((st = get_encoder()) != KD_OK) return st;
   const kd_kl_problem& p = *prob;
-  const FwdPlan f = plan_forward(p, di.num_sms);
+  const bool pair = use_pair();
+  const FwdPlan f = plan_forward(p, di.num_sms, pair, gemm_procs(di.num_sms, pair));
   if (workspace_bytes < f.total) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
@@ -369,7 +408,8 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
                               status, stream));
 
   CUtensorMap tmH, tmW;
-  if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW, W, d, V, d, BK, BN))
+  const int b_rows = f.pair ? LOGIT_BN / 2 : LOGIT_BN;  // W rows one CTA loads per tile
+  if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW, W, d, V, d, BK, b_rows))
     return KD_ERR_CUDA;
   GemmShape sh{};
   sh.inject_stall = inject_stall_from_env();
@@ -392,7 +432,8 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   ep.pm = at<float>(workspace, f.off_pm);
   ep.ps = at<float>(workspace, f.off_ps);
   ep.pd = at<float>(workspace, f.off_pd);
-  KD_CUDA(launch_gemm(GEMM_FWD_LSE, tmH, tmW, sh, ep, status, f.grid, stream));
+  if (log_plan()) print_plan("fwd_lse", f.pair, gemm_procs(di.num_sms, f.pair), sh, f.grid);
+  KD_CUDA(launch_gemm(GEMM_FWD_LSE, LOGIT_BN, f.pair, tmH, tmW, sh, ep, status, f.grid, stream));
 
   double* bsum = at<double>(workspace, f.off_bsum);
   KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, cl2, inv_tau, lse,
@@ -437,12 +478,21 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
   KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, T, K, V, inv_tau, sidx, sp, nullptr,
                               n_count, status, stream));
 
+  const bool pair = use_pair();
+  const int tile_m = pair ? 2 * BM : BM;
+  const int procs = gemm_procs(di.num_sms, pair);
+  const int cta_per_proc = pair ? 2 : 1;
   CUtensorMap tmH_K, tmW_K, tmW_MN, tmH_MN;
-  if (!encode_bf16_2d(&tmH_K, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW_K, W, d, V, d, BK, BN) ||
+  if (!encode_bf16_2d(&tmH_K, H, d, T, d, BK, BM) ||
+      !encode_bf16_2d(&tmW_K, W, d, V, d, BK, pair ? LOGIT_BN / 2 : LOGIT_BN) ||
       !encode_bf16_2d(&tmW_MN, W, d, V, d, 64, BK) || !encode_bf16_2d(&tmH_MN, H, d, T, d, 64, BK))
     return KD_ERR_CUDA;
 
-  const int dn_tiles = (int)ceil_div(d, BN);
+  // N tile of the dH / dW GEMMs (hidden dimension). 192-wide tiles avoid the
+  // zero-padded columns when d % 256 != 0 but measured slower on d = 2880
+  // (more operand bytes per MAC), so 256 is used throughout.
+  const int out_bn = 256;
+  const int dn_tiles = (int)ceil_div(d, out_bn);
   const int stall = inject_stall_from_env();
   for (int64_t tb = 0; tb < b.n_tblocks; ++tb) {
     const int row0 = (int)(tb * b.Tb);
@@ -456,9 +506,9 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
       {
         GemmShape sh{};
         sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(rows, BM);
-        sh.n_tiles = (int)ceil_div(cols, BN);
-        const SplitPlan spl = choose_split(sh.m_tiles, sh.n_tiles, di.num_sms, d);
+        sh.m_tiles = (int)ceil_div(rows, tile_m);
+        sh.n_tiles = (int)ceil_div(cols, LOGIT_BN);
+        const SplitPlan spl = choose_split(sh.m_tiles, sh.n_tiles, procs, d, tile_m);
         sh.nsplit = spl.nsplit;
         sh.group_n = spl.group_n;
         sh.units = sh.m_tiles * sh.nsplit;
@@ -481,8 +531,10 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         ep.g_over_tau = grad_loss * inv_tau;
         ep.G = Gbuf;
         ep.ldg = b.Vb_pad;
-        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
-        KD_CUDA(launch_gemm(GEMM_BWD_GRAD, tmH_K, tmW_K, sh, ep, status, grid, stream));
+        const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) print_plan("bwd_grad", pair, procs, sh, grid);
+        KD_CUDA(launch_gemm(GEMM_BWD_GRAD, LOGIT_BN, pair, tmH_K, tmW_K, sh, ep, status, grid,
+                            stream));
       }
       // 2) dH[rows] (+)= G . W[cols]
       {
@@ -490,7 +542,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM)) return KD_ERR_CUDA;
         GemmShape sh{};
         sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(rows, BM);
+        sh.m_tiles = (int)ceil_div(rows, tile_m);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
         sh.group_n = dn_tiles;
@@ -503,8 +555,9 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         ep.out_rows = rows;
         ep.out_cols = d;
         ep.accumulate = vb > 0 ? 1 : 0;
-        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
-        KD_CUDA(launch_gemm(GEMM_DH, tmG_K, tmW_MN, sh, ep, status, grid, stream));
+        const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) print_plan("dH", pair, procs, sh, grid);
+        KD_CUDA(launch_gemm(GEMM_DH, out_bn, pair, tmG_K, tmW_MN, sh, ep, status, grid, stream));
       }
       // 3) dW[cols] (+)= G^T . H[rows]
       {
@@ -512,7 +565,7 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         if (!encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK)) return KD_ERR_CUDA;
         GemmShape sh{};
         sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(cols, BM);
+        sh.m_tiles = (int)ceil_div(cols, tile_m);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
         sh.group_n = dn_tiles;
@@ -525,8 +578,9 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         ep.out_rows = cols;
         ep.out_cols = d;
         ep.accumulate = (accumulate_dW || tb > 0) ? 1 : 0;
-        const int grid = (int)std::min<int64_t>(sh.units, di.num_sms);
-        KD_CUDA(launch_gemm(GEMM_DW, tmG_MN, tmH_MN, sh, ep, status, grid, stream));
+        const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) print_plan("dW", pair, procs, sh, grid);
+        KD_CUDA(launch_gemm(GEMM_DW, out_bn, pair, tmG_MN, tmH_MN, sh, ep, status, grid, stream));
       }
     }
   }

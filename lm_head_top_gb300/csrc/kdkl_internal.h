@@ -28,6 +28,31 @@ cudaError_t launch_kernel(const char* name, void (*kern)(KArgs...), dim3 grid, d
   return e;
 }
 
+// Same, launched as clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                  size_t smem, cudaStream_t stream, unsigned cluster_x,
+                                  Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* token = nullptr;
+  note_launch_begin(name, stream, &token);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  note_launch_end(token, stream);
+  return e;
+}
+
 // kernels_small.cu
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
                                 int K, int V, float inv_tau, int32_t* sidx, float* sp, float* ent,
@@ -49,7 +74,14 @@ enum GemmKind {
   GEMM_DH = 2,        // A = G (K-major), B = W (MN-major), fp32 out
   GEMM_DW = 3         // A = G (MN-major), B = H (MN-major), fp32 out
 };
-cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// How many 2-CTA clusters of the GEMM kernel fit on the current device at once
+// (0 if unknown). The persistent grid must not exceed it.
+int pair_max_active_clusters();
+
+// bn: N tile width (LOGIT_BN for the logit GEMMs; 256 or 192 for dH/dW).
+// pair: 2-CTA clusters sharing one 256 x bn tile (grid must be even).
+cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB,
                         const GemmShape& sh, const EpiParams& ep, int* status, int grid,
                         cudaStream_t stream);
 

@@ -10,41 +10,90 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR>
 cudaError_t launch_one(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB,
                        const GemmShape& sh, const EpiParams& ep, int* status, int grid,
                        cudaStream_t stream) {
-  auto kern = tc_gemm_kernel<EPI, A_MN, B_MN>;
+  auto kern = tc_gemm_kernel<EPI, A_MN, B_MN, BN, PAIR>;
+  constexpr int smem = TileCfg<BN, PAIR>::SMEM_BYTES;
   static bool attr_done[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_kernel(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)GEMM_SMEM_BYTES,
-                       stream, tmA, tmB, sh, ep, status);
+  if (PAIR)
+    return launch_kernel_cluster(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)smem, stream,
+                                 2u, tmA, tmB, sh, ep, status);
+  return launch_kernel(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)smem, stream, tmA,
+                       tmB, sh, ep, status);
+}
+
+template <int EPI, bool A_MN, bool B_MN, int BN>
+cudaError_t launch_pick(bool pair, const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const GemmShape& sh, const EpiParams& ep, int* status, int grid,
+                        cudaStream_t stream) {
+  if (pair)
+    return launch_one<EPI, A_MN, B_MN, BN, true>(name, tmA, tmB, sh, ep, status, grid, stream);
+  return launch_one<EPI, A_MN, B_MN, BN, false>(name, tmA, tmB, sh, ep, status, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const GemmShape& sh, const EpiParams& ep, int* status, int grid,
-                        cudaStream_t stream) {
+int pair_max_active_clusters() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  // Every pair instantiation has the same block size and shared memory, so one
+  // of them stands for all.
+  auto kern = tc_gemm_kernel<EPI_LSE, false, false, LOGIT_BN, true>;
+  constexpr int smem = TileCfg<LOGIT_BN, true>::SMEM_BYTES;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB, const GemmShape& sh, const EpiParams& ep,
+                        int* status, int grid, cudaStream_t stream) {
+  if (pair && (grid % 2) != 0) return cudaErrorInvalidValue;
   switch (kind) {
     case GEMM_FWD_LSE:
-      return launch_one<EPI_LSE, false, false>("fwd_lse_gemm", tmA, tmB, sh, ep, status, grid,
-                                               stream);
+      if (bn != LOGIT_BN) break;
+      return launch_pick<EPI_LSE, false, false, LOGIT_BN>(pair, "fwd_lse_gemm", tmA, tmB, sh, ep,
+                                                          status, grid, stream);
     case GEMM_BWD_GRAD:
-      return launch_one<EPI_GRAD, false, false>("bwd_grad_gemm", tmA, tmB, sh, ep, status, grid,
-                                                stream);
+      if (bn != LOGIT_BN) break;
+      return launch_pick<EPI_GRAD, false, false, LOGIT_BN>(pair, "bwd_grad_gemm", tmA, tmB, sh,
+                                                           ep, status, grid, stream);
     case GEMM_DH:
-      return launch_one<EPI_STORE, false, true>("dH_gemm", tmA, tmB, sh, ep, status, grid, stream);
+      if (bn != 256) break;
+      return launch_pick<EPI_STORE, false, true, 256>(pair, "dH_gemm", tmA, tmB, sh, ep, status,
+                                                      grid, stream);
     case GEMM_DW:
-      return launch_one<EPI_STORE, true, true>("dW_gemm", tmA, tmB, sh, ep, status, grid, stream);
+      if (bn != 256) break;
+      return launch_pick<EPI_STORE, true, true, 256>(pair, "dW_gemm", tmA, tmB, sh, ep, status,
+                                                     grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -12,9 +12,10 @@
 //
 // Roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
-// Tiles are 128 x 256 with a 64-deep K step, 4 shared-memory stages, and two
-// 256-column fp32 accumulators in TMEM so the epilogue of one tile overlaps
-// the MMAs of the next.
+// Tiles are 128 x BN (BN = 256, or 192 for the dH/dW GEMMs when the hidden
+// size is a multiple of 192 but not of 256) with a 64-deep K step, 4-5
+// shared-memory stages, and two fp32 accumulators in TMEM so the epilogue of
+// one tile overlaps the MMAs of the next.
 //
 // Source of the method: "Efficient Knowledge Distillation for LLMs: Offline
 // Top-K Logits and a Fused Chunked KL Loss", page "Making knowledge
@@ -30,18 +31,31 @@
 namespace kdkl {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256;
+constexpr uint32_t TMEM_COLS = 512;  // two accumulators of up to 256 fp32 columns
 // MN-major operands arrive as 64-element-wide atoms of BK rows each.
 constexpr uint32_t MN_ATOM_BYTES = BK * 128;
+// N tile of the logit GEMMs (vocabulary direction).
+constexpr int LOGIT_BN = 256;
+
+// Shared-memory plan for an MMA tile of TILE_M x BN. With PAIR, two CTAs of a
+// cluster share one 256 x BN tile: each holds 128 rows of A and BN/2 rows of B
+// (so half the B bytes per CTA) and its own 128 x BN accumulator. As many
+// 64-deep stages as fit in ~200 KB, then the barriers.
+template <int BN, bool PAIR>
+struct TileCfg {
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows held by one CTA
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  // full, empty, tmem full x2, tmem empty x2, drain
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 512;
+};
 
 enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2 };
 
@@ -115,10 +129,17 @@ __device__ __forceinline__ int lower_bound_row(const int32_t* row, int K, int v)
   return lo;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmShape sh, const EpiParams ep, int* status) {
+  using Cfg = TileCfg<BN, PAIR>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int B_STAGE_BYTES = Cfg::B_STAGE_BYTES;
+  constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
+  constexpr int NUM_BARS = Cfg::NUM_BARS;
+  constexpr int TILE_M = Cfg::TILE_M;
+  constexpr int B_ROWS = Cfg::B_ROWS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -138,6 +159,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t limit = sh.inject_stall ? kInjectedWaitLimitNs : kWaitLimitNs;
+  // PAIR: CTAs 2c and 2c+1 form cluster c; rank 0 (the leader) issues the MMAs.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int group0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -146,7 +172,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), PAIR ? 8 : 4);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -156,50 +182,68 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
+      // Loads this CTA's A rows and B rows of every stage into its own shared
+      // memory. Single CTA: signals its own full barrier. Pair: both CTAs
+      // signal the LEADER's full barrier (pair form of the copy), which the
+      // leader arms with the bytes of both halves, so the leader's MMA thread
+      // waits on one barrier for the whole 256-row stage.
       int stage = 0;
       uint32_t phase = 0;
       long long fills = 0;
       bool ok = sh.inject_stall == 0;
-      for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+      const uint32_t full_leader0 = PAIR ? mapa_shared(full_bar(0), 0) : full_bar(0);
+      for (int u = group0; ok && u < sh.units; u += groups) {
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
+        const int a_row = sh.a_m0 + m * TILE_M + (int)rank * BM;
         for (int n = nb; ok && n < ne; ++n) {
+          const int b_row = sh.b_n0 + n * BN + (int)rank * B_ROWS;
           for (int kb = 0; kb < sh.k_blocks; ++kb) {
             if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status, limit)) {
               ok = false;
               break;
             }
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t fb = full_leader0 + 8u * stage;
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * STAGE_BYTES);
             const uint32_t a_dst = smem_u32(sA + stage * A_STAGE_BYTES);
             const uint32_t b_dst = smem_u32(sB + stage * B_STAGE_BYTES);
             const int kc = kb * BK;
+            auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+              if (PAIR)
+                tma_load_2d_pair(dst, tm, fb, x, y);
+              else
+                tma_load_2d(dst, tm, fb, x, y);
+            };
             if (!A_MN) {
-              tma_load_2d(a_dst, &tmA, fb, sh.a_k0 + kc, sh.a_m0 + m * BM);
+              load(a_dst, &tmA, sh.a_k0 + kc, a_row);
             } else {
 #pragma unroll
               for (int a = 0; a < BM / 64; ++a)
-                tma_load_2d(a_dst + a * MN_ATOM_BYTES, &tmA, fb, sh.a_m0 + m * BM + 64 * a,
-                            sh.a_k0 + kc);
+                load(a_dst + a * MN_ATOM_BYTES, &tmA, a_row + 64 * a, sh.a_k0 + kc);
             }
             if (!B_MN) {
-              tma_load_2d(b_dst, &tmB, fb, sh.b_k0 + kc, sh.b_n0 + n * BN);
+              load(b_dst, &tmB, sh.b_k0 + kc, b_row);
             } else {
 #pragma unroll
-              for (int a = 0; a < BN / 64; ++a)
-                tma_load_2d(b_dst + a * MN_ATOM_BYTES, &tmB, fb, sh.b_n0 + n * BN + 64 * a,
-                            sh.b_k0 + kc);
+              for (int a = 0; a < B_ROWS / 64; ++a)
+                load(b_dst + a * MN_ATOM_BYTES, &tmB, b_row + 64 * a, sh.b_k0 + kc);
             }
             ++fills;
             if (++stage == STAGES) {
@@ -209,24 +253,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      // Teardown: every issued copy must have landed before the CTA exits.
-      for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f)
-        mbar_drain_bounded(full_bar((int)(f % STAGES)), (uint32_t)((f / STAGES) & 1));
+      // Teardown: every copy issued must have landed before the CTA exits. The
+      // full barriers live in the leader and count both halves of the pair,
+      // so the leader drains for both; the peer's copies are also covered by
+      // the closing cluster barrier, which the leader reaches only after its
+      // MMAs consumed every stage.
+      if (leader)
+        for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f)
+          mbar_drain_bounded(full_bar((int)(f % STAGES)), (uint32_t)((f / STAGES) & 1));
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+      for (int u = group0; ok && u < sh.units; u += groups) {
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
-          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status, limit)) {
+          const bool freed = PAIR ? mbar_wait_cluster_bounded(tempty_bar(acc), acc_phase ^ 1u,
+                                                              abort_flag, status, limit)
+                                  : mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u,
+                                                      abort_flag, status, limit);
+          if (!freed) {
             ok = false;
             break;
           }
@@ -246,22 +299,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                        : sdesc_sw128(a_base + k * 32, 16, 1024);
               const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                        : sdesc_sw128(b_base + k * 32, 16, 1024);
-              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              if (PAIR)
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
-            tc_commit(empty_bar(stage));
+            if (PAIR)
+              tc_commit_pair_multicast(empty_bar(stage), 0x3);
+            else
+              tc_commit(empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          tc_commit(tfull_bar(acc));
+          if (PAIR)
+            tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+          else
+            tc_commit(tfull_bar(acc));
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
       // Teardown: all MMAs issued by this thread complete before TMEM is freed.
-      tc_commit(drain_bar);
+      if (PAIR)
+        tc_commit_pair_local(drain_bar);
+      else
+        tc_commit(drain_bar);
       mbar_drain_bounded(drain_bar, 0);
     }
   } else {
@@ -272,10 +337,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sh.units; u += gridDim.x) {
+    const uint32_t tempty_remote0 = PAIR ? mapa_shared(tempty_bar(0), 0) : 0u;
+    for (int u = group0; ok && u < sh.units; u += groups) {
       int m, s, nb, ne;
       unit_coords(sh, u, m, s, nb, ne);
-      const int r = m * BM + r_in_tile;  // row within this launch
+      const int r = m * TILE_M + (int)rank * BM + r_in_tile;  // row within this launch
       // per-unit row state
       float run_max = -INFINITY, run_sum = 0.f, dot = 0.f;
       float lse2 = 0.f, scale = 0.f;
@@ -395,7 +461,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(tempty_remote0 + 8u * acc);  // the leader's barrier
+          else
+            mbar_arrive(tempty_bar(acc));
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -411,10 +482,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the leader's MMAs into the peer's TMEM are done
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

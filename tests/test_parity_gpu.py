@@ -63,6 +63,9 @@ def test_small_workload(kdkl):
     (64, 32, 48, 48, 16, 0.5),
     # K = 512 (largest), V just above
     (40, 48, 600, 512, 7, 1.0),
+    # hidden sizes that take 192-wide dH / dW tiles (multiple of 192, not of 256)
+    (200, 576, 900, 10, 70, 1.0),
+    (129, 384, 777, 3, 129, 1.5),
 ])
 def test_ragged_shapes(kdkl, shape):
     T, d, V, K, chunk, tau = shape

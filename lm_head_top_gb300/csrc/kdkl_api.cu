@@ -29,7 +29,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/kdkl.h"
+#include "kdkl.h"
 #include "kdkl_internal.h"
 #include "tc_gemm.cuh"
 
@@ -158,11 +158,18 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct SplitPlan {
   int nsplit, group_n;
 };
-constexpr double kL2RowBudget = 24.0 * 1024 * 1024;
+constexpr double kL2RowBudgetDefault = 24.0 * 1024 * 1024;
+
+// KDKL_L2_ROWS_MB overrides the L2 budget for the A rows of one group (tuning).
+double l2_row_budget() {
+  const char* v = getenv("KDKL_L2_ROWS_MB");
+  const double mb = v ? atof(v) : 0.0;
+  return mb > 0 ? mb * 1024 * 1024 : kL2RowBudgetDefault;
+}
 
 SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d, int tile_m) {
   const double a_tile_bytes = (double)tile_m * (double)d * 2.0;
-  int gm = (int)std::max(1.0, std::floor(kL2RowBudget / a_tile_bytes));
+  int gm = (int)std::max(1.0, std::floor(l2_row_budget() / a_tile_bytes));
   gm = std::min(gm, m_tiles);
   int group_n = (num_sms + gm - 1) / gm;
   group_n = std::max(1, std::min(group_n, n_tiles));

@@ -18,7 +18,7 @@
 
 #include <mutex>
 
-#include "../../include/kdkl.h"
+#include "kdkl.h"
 
 namespace {
 

@@ -445,15 +445,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 if (4 * j < nvalid) {
-                  float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                  if (ep.accumulate) {
-                    const float4 prev = *reinterpret_cast<const float4*>(dst + 4 * j);
-                    o.x += prev.x;
-                    o.y += prev.y;
-                    o.z += prev.z;
-                    o.w += prev.w;
-                  }
-                  *reinterpret_cast<float4*>(dst + 4 * j) = o;
+                  const float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                  // Accumulate with a vector reduction: every element gets
+                  // exactly one add per launch and launches are stream-ordered,
+                  // so the sum order is fixed (deterministic).
+                  if (ep.accumulate)
+                    red_add_f32x4(dst + 4 * j, o);
+                  else
+                    *reinterpret_cast<float4*>(dst + 4 * j) = o;
                 }
               }
             }

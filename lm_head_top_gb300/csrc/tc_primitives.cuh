@@ -341,6 +341,13 @@ __device__ __forceinline__ float select32(const float (&v)[32], int i) {
   return r;
 }
 
+// out[0..3] += v (one vector reduction in L2; no value comes back).
+__device__ __forceinline__ void red_add_f32x4(float* out, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const uint32_t a = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo));
   const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi));

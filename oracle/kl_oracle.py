@@ -205,3 +205,24 @@ def dW_rows(H, W, topk_idx, topk_logit, mask, tau: float, vocab_rows, lse,
         return np.zeros((len(vs), H.shape[1]))
     G = (q - P) * (grad_loss * m / (tau * n))[:, None]
     return G.T @ H
+
+
+# --------------------------------------------------------------------------
+# Offline teacher cache: the top-K (id, logit) pairs of each row of z = H W^T.
+# ("Making knowledge distillation cheap enough to run at scale", section "Two
+# system changes": compute the teacher's output once and cache the 100 most
+# likely tokens per position.) Order: logit descending, ties by smaller id.
+
+def topk_logits(H, W, K: int):
+    """(ids [T,K] int64, logits [T,K] fp64) from the dense fp64 grid z = H W^T,
+    each row sorted by (logit descending, id ascending)."""
+    z = student_logits(H, W)
+    T, V = z.shape
+    if not 1 <= K <= V:
+        raise ValueError("need 1 <= K <= V")
+    ids = np.empty((T, K), dtype=np.int64)
+    for t in range(T):
+        # lexsort: last key is primary; -z descending, then id ascending
+        order = np.lexsort((np.arange(V), -z[t]))
+        ids[t] = order[:K]
+    return ids, np.take_along_axis(z, ids, axis=1)

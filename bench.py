@@ -337,6 +337,78 @@ def run_kdkl(args):
     return result
 
 
+def run_topk(args):
+    """The offline top-K cache producer on the same head shapes: the teacher's
+    K = 100 largest logits per token over V = 201,088 (no logit grid stored)."""
+    from lm_head_top_gb300 import kdkl
+    from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    kdkl.load()
+    w = WORKLOADS[args.workload].with_(teacher="uniform")
+    if args.tokens:
+        w = w.with_(T=args.tokens)
+    x = make_inputs(w, seed=rank)
+    T, d, V, K = w.T, w.d, w.V, 100
+    torch.cuda.reset_peak_memory_stats(dev)
+    H, W = x["H"].to(dev), x["W"].to(dev)
+    ws = torch.empty(kdkl.kd_lmhead_topk_workspace_size(T, d, V, K), dtype=torch.uint8, device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    val = torch.empty(T, K, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kdkl.kd_lmhead_topk(H, W, K, topk_idx=idx, topk_logit=val, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kdkl.kd_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        kdkl.kd_timing_begin()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_kernel = kdkl.kd_timing_end()
+        barrier(world)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    rows = {n: (c, ms) for n, c, ms in per_kernel}
+    c, ms = rows["topk_gemm"]
+    flops = 2.0 * T * V * d
+    achieved = flops / (ms / c / 1e3) / 1e12  # one topk_gemm launch per step
+    return {
+        "metric": "offline top-K teacher cache (LM head x top-100) tokens/s", "path": "topk",
+        "value": round(T * world * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s_topk" % w.name, "T": T, "d": d, "V": V, "K": K,
+                   "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
+        "tflops": round(flops * args.steps / (elapsed_ms / 1e3) / 1e12, 1),
+        "peak_hbm_gib": round(torch.cuda.max_memory_allocated(dev) / 2 ** 30, 3),
+        "roofline": {"bound": "tensor", "kernel": "topk_gemm", "achieved": round(achieved, 1),
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
+                     "peak_source": "%s bf16_tflops_sustained" % pk_src,
+                     "traffic": recorded_traffic("topk_gemm")},
+        "gpu_launches": kdkl.kd_launch_count() - launches0,
+        "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
+        "clocks": clocks.summary(),
+    }
+
+
 def run_reference(args):
     """The fp64 CPU oracle on bounded token samples of the same workload."""
     from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
@@ -374,6 +446,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("kdkl", "reference"), default="kdkl")
+    ap.add_argument("--path", choices=("kl", "topk"), default="kl",
+                    help="kl: fused KL fwd+bwd (the headline); topk: offline top-K cache producer")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -384,7 +458,12 @@ def main():
     args = ap.parse_args()
     if args.impl == "kdkl":
         args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
-    res = run_reference(args) if args.impl == "reference" else run_kdkl(args)
+    if args.impl == "reference":
+        res = run_reference(args)
+    elif args.path == "topk":
+        res = run_topk(args)
+    else:
+        res = run_kdkl(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -131,6 +131,40 @@ kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, co
                                 const uint8_t* mask, float* loss, float* lse, float* token_kl,
                                 void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Offline teacher cache producer: for every row t of H, the K largest logits
+ * z[t,v] = H[t] . W[v] over the full vocabulary, with their ids. This is the
+ * cache the loss above consumes ("Making knowledge distillation cheap enough
+ * to run at scale", section "Two system changes": compute the teacher's
+ * output once and cache the 100 most likely tokens per position). The same
+ * tensor-core GEMM produces each logit tile; its epilogue keeps per-row
+ * candidate lists above a running threshold, so the logits are never stored.
+ */
+#define KDKL_TOPK_MAX_K 256
+
+typedef struct {
+  int64_t T;   /* rows of H (tokens) */
+  int64_t d;   /* hidden size; multiple of 8 */
+  int64_t V;   /* vocabulary (rows of W) */
+  int32_t K;   /* entries kept per row, 1..min(V, KDKL_TOPK_MAX_K) */
+  int32_t reserved;  /* set to 0 */
+} kd_topk_problem;
+
+/* Workspace bytes for kd_lmhead_topk; linear in T; 0 if the problem is invalid. */
+size_t kd_lmhead_topk_workspace_size(const kd_topk_problem* prob);
+
+/*   H          [T, d] bf16      hidden states (device)
+ *   W          [V, d] bf16      output projection (device)
+ *   topk_idx   [T, K] int32 out ids, per row by logit descending, ties to the smaller id
+ *   topk_logit [T, K] fp32 out  the logits z (fp32 accumulation of the bf16 products)
+ * Errors: KD_ERR_SHAPE (T < 0, d < 8, V < 1, K outside 1..min(V, KDKL_TOPK_MAX_K)),
+ * KD_ERR_ALIGNMENT (d % 8 != 0 or misaligned pointers), KD_ERR_INVALID_ARG (null
+ * pointers), KD_ERR_WORKSPACE, KD_ERR_CUDA, KD_ERR_UNSUPPORTED; device-detected
+ * errors via kd_kl_check_status(workspace). */
+kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const uint16_t* W,
+                         int32_t* topk_idx, float* topk_logit, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* BLOCKING: synchronises `stream`, then returns the first device-detected
  * error recorded in `workspace` by the latest call that used it (KD_OK if
  * none). Each forward/backward call clears the record when it starts. */

@@ -5,5 +5,6 @@ The compute path is the CUDA library ``libkdkl.so`` (C ABI in
 synthetic input generator.
 """
 from .kdkl import (KDKLError, kd_kl_backward, kd_kl_check_status, kd_kl_forward,  # noqa: F401
-                   kd_kl_workspace_size, kd_launch_count, kd_status_string, kd_timing_begin,
+                   kd_kl_workspace_size, kd_launch_count, kd_lmhead_topk,
+                   kd_lmhead_topk_workspace_size, kd_status_string, kd_timing_begin,
                    kd_timing_end)

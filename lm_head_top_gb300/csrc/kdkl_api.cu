@@ -269,6 +269,48 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
   return b;
 }
 
+// ---- offline top-K producer
+constexpr int kTopkMergeMax = 4096;  // nsplit * K entries sorted per row by the merge
+
+struct TopkPlan {
+  bool pair;
+  int m_tiles, n_tiles, nsplit, group_n, grid, cap;
+  size_t off_cand_val, off_cand_id, off_unit_val, off_unit_id, total;
+};
+
+bool topk_problem_ok(const kd_topk_problem* p) {
+  return p && p->T >= 0 && p->T < (1ll << 31) && p->d >= 8 && p->d < (1ll << 31) &&
+         p->d % 8 == 0 && p->V >= 1 && p->V < (1ll << 31) && p->K >= 1 &&
+         p->K <= KDKL_TOPK_MAX_K && (int64_t)p->K <= p->V;
+}
+
+TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) {
+  TopkPlan f{};
+  const int tile_m = pair ? 2 * BM : BM;
+  f.pair = pair;
+  f.m_tiles = (int)std::max<int64_t>(ceil_div(p.T, tile_m), 1);
+  f.n_tiles = (int)ceil_div(p.V, LOGIT_BN);
+  SplitPlan sp = choose_split(f.m_tiles, f.n_tiles, procs, p.d, tile_m);
+  const int max_ns = std::max(1, std::min(f.n_tiles, kTopkMergeMax / p.K));
+  if (sp.nsplit > max_ns) {
+    sp.nsplit = max_ns;
+    sp.group_n = std::min(sp.group_n, max_ns);
+  }
+  f.nsplit = sp.nsplit;
+  f.group_n = sp.group_n;
+  f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
+  f.cap = p.K + 256;
+  const size_t cand = (size_t)num_sms * BM * f.cap;  // one list per (CTA, row), any grid <= SMs
+  const size_t unit = (size_t)f.nsplit * p.T * p.K;
+  size_t o = kHeaderBytes;
+  f.off_cand_val = o; o = align256(o + cand * 4);
+  f.off_cand_id = o; o = align256(o + cand * 4);
+  f.off_unit_val = o; o = align256(o + unit * 4);
+  f.off_unit_id = o; o = align256(o + unit * 4);
+  f.total = o;
+  return f;
+}
+
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // GEMM tiling mode: 2-CTA pairs (cta_group::2, 256-row tiles, half the B
@@ -592,6 +634,72 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
     }
   }
   KD_CUDA(launch_f32_to_bf16(dH_acc, dH, (long long)p.T * p.d, di.num_sms, stream));
+  return KD_OK;
+}
+
+size_t kd_lmhead_topk_workspace_size(const kd_topk_problem* prob) {
+  if (!topk_problem_ok(prob)) return 0;
+  DeviceInfo di;
+  const int sms = (device_info(&di) == KD_OK) ? di.num_sms : 160;
+  size_t total = plan_topk(*prob, sms, false, sms).total;
+  for (int procs = 1; procs <= sms / 2; ++procs)
+    total = std::max(total, plan_topk(*prob, sms, true, procs).total);
+  return total;
+}
+
+kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const uint16_t* W,
+                         int32_t* topk_idx, float* topk_logit, void* workspace,
+                         size_t workspace_bytes, void* stream_ptr) {
+  if (!prob) return KD_ERR_INVALID_ARG;
+  if (!topk_problem_ok(prob)) return (prob->d % 8 != 0 && prob->d >= 8) ? KD_ERR_ALIGNMENT
+                                                                        : KD_ERR_SHAPE;
+  if (!workspace) return KD_ERR_WORKSPACE;
+  if (!W || (prob->T > 0 && (!H || !topk_idx || !topk_logit))) return KD_ERR_INVALID_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(workspace, 16) || !aligned(topk_idx, 4) ||
+      !aligned(topk_logit, 4))
+    return KD_ERR_ALIGNMENT;
+  DeviceInfo di;
+  kd_status st;
+  if ((st = device_info(&di)) != KD_OK) return st;
+  if ((st = get_encoder()) != KD_OK) return st;
+  const kd_topk_problem& p = *prob;
+  const bool pair = use_pair();
+  const int procs = gemm_procs(di.num_sms, pair);
+  const TopkPlan f = plan_topk(p, di.num_sms, pair, procs);
+  if (workspace_bytes < f.total) return KD_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int* status = at<int>(workspace, 0);
+  KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
+  if (p.T == 0) return KD_OK;
+  const int T = (int)p.T, d = (int)p.d, V = (int)p.V, K = p.K;
+
+  CUtensorMap tmH, tmW;
+  if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) ||
+      !encode_bf16_2d(&tmW, W, d, V, d, BK, pair ? LOGIT_BN / 2 : LOGIT_BN))
+    return KD_ERR_CUDA;
+  GemmShape sh{};
+  sh.inject_stall = inject_stall_from_env();
+  sh.m_tiles = f.m_tiles;
+  sh.n_tiles = f.n_tiles;
+  sh.nsplit = f.nsplit;
+  sh.group_n = f.group_n;
+  sh.units = f.m_tiles * f.nsplit;
+  sh.k_blocks = (int)ceil_div(d, BK);
+  EpiParams ep{};
+  ep.K = K;
+  ep.T = T;
+  ep.row0 = 0;
+  ep.rows = T;
+  ep.col0 = 0;
+  ep.cols = V;
+  ep.topk_cap = f.cap;
+  ep.cand_val = at<float>(workspace, f.off_cand_val);
+  ep.cand_id = at<int32_t>(workspace, f.off_cand_id);
+  ep.unit_val = at<float>(workspace, f.off_unit_val);
+  ep.unit_id = at<int32_t>(workspace, f.off_unit_id);
+  if (log_plan()) print_plan("topk", pair, procs, sh, f.grid);
+  KD_CUDA(launch_gemm(GEMM_TOPK, LOGIT_BN, pair, tmH, tmW, sh, ep, status, f.grid, stream));
+  KD_CUDA(launch_topk_merge(ep.unit_val, ep.unit_id, f.nsplit, T, K, topk_idx, topk_logit, stream));
   return KD_OK;
 }
 

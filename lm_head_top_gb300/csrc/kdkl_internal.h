@@ -66,13 +66,18 @@ cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const in
                                  float* loss, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
                                cudaStream_t stream);
+// merge of per-split top-K lists; shared memory = topk_merge_p2() * 8 bytes
+int topk_merge_p2(int nsplit, int K);
+cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, int nsplit, int T, int K,
+                              int32_t* out_id, float* out_val, cudaStream_t stream);
 
 // kernels_gemm.cu — tcgen05 GEMMs (see tc_gemm.cuh for the epilogues)
 enum GemmKind {
   GEMM_FWD_LSE = 0,   // A = H (K-major), B = W (K-major), online logsumexp + gather
   GEMM_BWD_GRAD = 1,  // A = H (K-major), B = W (K-major), softmax - P into the bf16 buffer
   GEMM_DH = 2,        // A = G (K-major), B = W (MN-major), fp32 out
-  GEMM_DW = 3         // A = G (MN-major), B = H (MN-major), fp32 out
+  GEMM_DW = 3,        // A = G (MN-major), B = H (MN-major), fp32 out
+  GEMM_TOPK = 4       // A = H (K-major), B = W (K-major), per-split top-K lists
 };
 // How many 2-CTA clusters of the GEMM kernel fit on the current device at once
 // (0 if unknown). The persistent grid must not exceed it.

@@ -86,6 +86,10 @@ cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA
       if (bn != LOGIT_BN) break;
       return launch_pick<EPI_GRAD, false, false, LOGIT_BN>(pair, "bwd_grad_gemm", tmA, tmB, sh,
                                                            ep, status, grid, stream);
+    case GEMM_TOPK:
+      if (bn != LOGIT_BN) break;
+      return launch_pick<EPI_TOPK, false, false, LOGIT_BN>(pair, "topk_gemm", tmA, tmB, sh, ep,
+                                                           status, grid, stream);
     case GEMM_DH:
       if (bn != 256) break;
       return launch_pick<EPI_STORE, false, true, 256>(pair, "dH_gemm", tmA, tmB, sh, ep, status,

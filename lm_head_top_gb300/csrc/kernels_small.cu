@@ -175,6 +175,57 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
   }
 }
 
+// Merge each row's per-split top-K lists into the row's top-K, sorted by
+// (logit descending, id ascending). One block per row; the nsplit x K entries
+// are sorted as 64-bit keys (inverted order key of the logit, then the id) by
+// a block-wide bitonic sort in shared memory (p2 = next power of two >= nsplit*K).
+__device__ __forceinline__ uint32_t merge_order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(256)
+    topk_merge_kernel(const float* __restrict__ unit_val, const int32_t* __restrict__ unit_id,
+                      int nsplit, int T, int K, int p2, int32_t* __restrict__ out_id,
+                      float* __restrict__ out_val) {
+  extern __shared__ unsigned long long mkeys[];
+  const int t = blockIdx.x;
+  const int n = nsplit * K;
+  for (int e = threadIdx.x; e < p2; e += blockDim.x) {
+    unsigned long long key = ~0ull;
+    if (e < n) {
+      const int s = e / K, k = e - (e / K) * K;
+      const long long o = ((long long)s * T + t) * K + k;
+      const float v = unit_val[o];
+      const int32_t id = unit_id[o];
+      key = ((unsigned long long)(~merge_order_key(v)) << 32) | (uint32_t)id;
+    }
+    mkeys[e] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= p2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (p2 >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool ascending = (lo & size) == 0;
+        const unsigned long long a = mkeys[lo], b = mkeys[hi];
+        if ((a > b) == ascending) {
+          mkeys[lo] = b;
+          mkeys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const unsigned long long key = mkeys[k];
+    const uint32_t ok = ~(uint32_t)(key >> 32);
+    out_val[(long long)t * K + k] = __uint_as_float((ok & 0x80000000u) ? (ok & 0x7fffffffu) : ~ok);
+    out_id[(long long)t * K + k] = (int32_t)(uint32_t)(key & 0xffffffffu);
+  }
+}
+
 // ------------------------------------------------------------ host launchers
 
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
@@ -205,6 +256,20 @@ cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const in
                                  float* loss, cudaStream_t stream) {
   return launch_kernel("loss_finalize", loss_finalize_kernel, dim3(1), dim3(1024), 0, stream,
                        block_sums, nblocks, n_count, loss);
+}
+
+int topk_merge_p2(int nsplit, int K) {
+  int p2 = 1;
+  while (p2 < nsplit * K) p2 <<= 1;
+  return p2 < 2 ? 2 : p2;
+}
+
+cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, int nsplit, int T, int K,
+                              int32_t* out_id, float* out_val, cudaStream_t stream) {
+  const int p2 = topk_merge_p2(nsplit, K);
+  return launch_kernel("topk_merge", topk_merge_kernel, dim3(T), dim3(256),
+                       (size_t)p2 * sizeof(unsigned long long), stream, unit_val, unit_id, nsplit,
+                       T, K, p2, out_id, out_val);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,

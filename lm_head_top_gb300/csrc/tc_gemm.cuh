@@ -57,7 +57,7 @@ struct TileCfg {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 512;
 };
 
-enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2 };
+enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2, EPI_TOPK = 3 };
 
 // Work decomposition: `units` = m_tiles * nsplit. A unit is one m-tile and one
 // split (a contiguous range of n-tiles). Units are numbered group by group:
@@ -105,7 +105,80 @@ struct EpiParams {
   int64_t ldo;
   int out_rows, out_cols;
   int accumulate;
+  // EPI_TOPK (K is the field above)
+  int topk_cap;      // capacity of a row's candidate list (K + 256, at most 512)
+  float* cand_val;   // [gridDim.x * BM, topk_cap] candidate logits, one list per (CTA, row)
+  int32_t* cand_id;  // same shape, vocabulary ids
+  float* unit_val;   // [nsplit, T, K] each split's top-K per row (id order)
+  int32_t* unit_id;
 };
+
+// Order-preserving map of an fp32 value to uint32 (larger float, larger key).
+__device__ __forceinline__ uint32_t f32_order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float f32_from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The whole warp reduces one row's candidate list (n entries, n >= K, at most
+// 512, appended in increasing id order) to its K best by (logit descending, id
+// ascending), in place and in the same id order. Returns the K-th best logit,
+// the row's new admission threshold: a later candidate of the same row has a
+// larger id, so only a strictly larger logit can displace a kept entry.
+// The K-th largest key is found by bisection over the 32-bit order keys.
+static __device__ __noinline__ float topk_compact_row(float* vals, int32_t* ids, int n, int K) {
+  constexpr int MAXE = 16;  // 512 entries / 32 lanes
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  uint32_t key[MAXE];
+  int32_t idv[MAXE];
+#pragma unroll
+  for (int i = 0; i < MAXE; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = e < n ? f32_order_key(vals[e]) : 0u;
+    idv[i] = e < n ? ids[e] : -1;
+  }
+  uint32_t lo = 0u, hi = 0xffffffffu;
+  while (lo < hi) {
+    const uint32_t mid = lo + ((hi - lo) >> 1) + 1u;
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) c += (i * 32 + lane < n && key[i] >= mid) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (c >= K) lo = mid; else hi = mid - 1u;
+  }
+  int gt = 0;
+#pragma unroll
+  for (int i = 0; i < MAXE; ++i) gt += (i * 32 + lane < n && key[i] > lo) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
+  const int need_eq = K - gt;
+  __syncwarp();
+  int written = 0, eq_seen = 0;
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < MAXE; ++i) {
+    const bool valid = i * 32 + lane < n;
+    const bool is_gt = valid && key[i] > lo;
+    const bool is_eq = valid && key[i] == lo;
+    const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
+    const int eq_rank = eq_seen + __popc(eq_mask & below);
+    const bool keep = is_gt || (is_eq && eq_rank < need_eq);
+    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int pos = written + __popc(keep_mask & below);
+      vals[pos] = f32_from_order_key(key[i]);
+      ids[pos] = idv[i];
+    }
+    written += __popc(keep_mask);
+    eq_seen += __popc(eq_mask);
+  }
+  __syncwarp();
+  return f32_from_order_key(lo);
+}
 
 __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
                                             int& ne) {
@@ -349,6 +422,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int32_t* id_row = nullptr;
       const float* p_row = nullptr;
       bool row_ok = false;
+      // EPI_TOPK row state: admission threshold and candidate count
+      float th = INFINITY;
+      int cnt = 0;
+      float* c_val = nullptr;
+      int32_t* c_id = nullptr;
+      if (EPI == EPI_TOPK) {
+        row_ok = r < ep.rows;
+        th = row_ok ? -INFINITY : INFINITY;
+        const long long slot = ((long long)blockIdx.x * BM + r_in_tile) * ep.topk_cap;
+        c_val = ep.cand_val + slot;
+        c_id = ep.cand_id + slot;
+      }
       if (EPI == EPI_LSE || EPI == EPI_GRAD) {
         row_ok = r < ep.rows;
         if (row_ok) {
@@ -377,10 +462,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           const int cl = n * BN + c * 32;  // column within this launch
-          if (EPI == EPI_LSE || EPI == EPI_GRAD) {
+          if (EPI == EPI_LSE || EPI == EPI_GRAD || EPI == EPI_TOPK) {
             if (cl >= ep.cols) break;  // warp-uniform
           } else {
             if (cl >= ep.out_cols) break;
+          }
+          if (EPI == EPI_TOPK) {
+            // room for this piece's 32 possible appends in every row of the warp
+            uint32_t need = __ballot_sync(0xffffffffu, cnt > ep.topk_cap - 32);
+            while (need) {
+              const int i = __ffs(need) - 1;
+              need &= need - 1u;
+              const int ni = __shfl_sync(0xffffffffu, cnt, i);
+              const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
+              const float thi = topk_compact_row(ep.cand_val + slot_i, ep.cand_id + slot_i, ni, ep.K);
+              if (lane == i) {
+                th = thi;
+                cnt = ep.K;
+              }
+            }
           }
           float v[32];
           __syncwarp();
@@ -438,6 +538,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 dst[j] = w;
               }
             }
+          } else if (EPI == EPI_TOPK) {
+            const int vid0 = ep.col0 + cl;
+            const int nv = min(32, ep.cols - cl);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j < nv && v[j] > th) {
+                c_val[cnt] = v[j];
+                c_id[cnt] = vid0 + j;
+                ++cnt;
+              }
+            }
           } else {  // EPI_STORE
             if (r < ep.out_rows) {
               float* dst = ep.out + (long long)r * ep.ldo + cl;
@@ -470,6 +581,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) break;
+      if (EPI == EPI_TOPK) {
+        // final reduction to the split's top-K of every row, then write it out
+        uint32_t need = __ballot_sync(0xffffffffu, cnt > ep.K);
+        while (need) {
+          const int i = __ffs(need) - 1;
+          need &= need - 1u;
+          const int ni = __shfl_sync(0xffffffffu, cnt, i);
+          const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
+          topk_compact_row(ep.cand_val + slot_i, ep.cand_id + slot_i, ni, ep.K);
+          if (lane == i) cnt = ep.K;
+        }
+        if (row_ok) {
+          const long long o = ((long long)s * ep.T + ep.row0 + r) * ep.K;
+          for (int k = 0; k < ep.K; ++k) {
+            ep.unit_val[o + k] = k < cnt ? c_val[k] : -INFINITY;
+            ep.unit_id[o + k] = k < cnt ? c_id[k] : -1;
+          }
+        }
+      }
       if (EPI == EPI_LSE && row_ok) {
         const long long o = (long long)s * ep.T + ep.row0 + r;
         ep.pm[o] = run_max;

@@ -36,6 +36,14 @@ class kd_kl_problem(ctypes.Structure):
                 ("K", ctypes.c_int32), ("temperature", ctypes.c_float), ("chunk", ctypes.c_int64)]
 
 
+class kd_topk_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("K", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+KDKL_TOPK_MAX_K = 256
+
+
 class kd_kernel_time(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -52,6 +60,9 @@ _SIGS = {
                                       _P]),
     "kd_kl_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
                                              _P, _P, _P, _P]),
+    "kd_lmhead_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_topk_problem)]),
+    "kd_lmhead_topk": (ctypes.c_int, [ctypes.POINTER(kd_topk_problem), _P, _P, _P, _P, _P,
+                                      ctypes.c_size_t, _P]),
     "kd_kl_check_status": (ctypes.c_int, [_P, _P]),
     "kd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kd_launch_count": (ctypes.c_int64, []),
@@ -215,6 +226,38 @@ def kd_kl_forward_noalloc(H, W, topk_idx, topk_logit, mask=None, *, temperature=
     if rc != KD_OK:
         raise KDKLError(rc, "kd_kl_forward_noalloc")
     return loss, lse, token_kl
+
+
+def kd_lmhead_topk_workspace_size(T, d, V, K) -> int:
+    p = kd_topk_problem(int(T), int(d), int(V), int(K), 0)
+    return int(load().kd_lmhead_topk_workspace_size(ctypes.byref(p)))
+
+
+def kd_lmhead_topk(H, W, K, *, topk_idx=None, topk_logit=None, workspace=None, stream=None):
+    """Offline teacher cache: the K largest logits of each row of H . W^T and
+    their ids, per row by logit descending (ties: smaller id first).
+    Returns (topk_idx [T,K] int32, topk_logit [T,K] fp32)."""
+    T, d = H.shape
+    V = W.shape[0]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    dev = H.device
+    p = kd_topk_problem(int(T), int(d), int(V), int(K), 0)
+    need = int(load().kd_lmhead_topk_workspace_size(ctypes.byref(p)))
+    if need == 0:
+        raise KDKLError(2, "kd_lmhead_topk_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if topk_logit is None:
+        topk_logit = torch.empty((T, K), dtype=torch.float32, device=dev)
+    rc = load().kd_lmhead_topk(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
+                               _ptr(topk_logit), _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_lmhead_topk")
+    return topk_idx, topk_logit
 
 
 def kd_kl_check_status(workspace: torch.Tensor, stream=None) -> int:

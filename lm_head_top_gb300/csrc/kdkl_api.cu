@@ -270,12 +270,26 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
 }
 
 // ---- offline top-K producer
+
+
 constexpr int kTopkMergeMax = 4096;  // nsplit * K entries sorted per row by the merge
+constexpr int kTopkSlackDefault = 512;  // i.e. the full 512-entry list
+
+// Candidate-list room above K before a row's list is compacted (at least 64;
+// the list holds at most 512). Smaller slack compacts more often and raises
+// the shared thresholds sooner, larger slack compacts less often;
+// KDKL_TOPK_SLACK overrides the default (tuning).
+int topk_slack() {
+  const char* v = getenv("KDKL_TOPK_SLACK");
+  int s = v ? atoi(v) : 0;
+  if (s <= 0) s = kTopkSlackDefault;
+  return std::max(64, std::min(512, s));
+}
 
 struct TopkPlan {
   bool pair;
   int m_tiles, n_tiles, nsplit, group_n, grid, cap;
-  size_t off_cand_val, off_cand_id, off_unit_val, off_unit_id, total;
+  size_t off_cand, off_row_key, off_unit_val, off_unit_id, total;
 };
 
 bool topk_problem_ok(const kd_topk_problem* p) {
@@ -299,12 +313,12 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   f.nsplit = sp.nsplit;
   f.group_n = sp.group_n;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
-  f.cap = p.K + 256;
+  f.cap = std::max(p.K + 64, std::min(512, p.K + topk_slack()));
   const size_t cand = (size_t)num_sms * BM * f.cap;  // one list per (CTA, row), any grid <= SMs
   const size_t unit = (size_t)f.nsplit * p.T * p.K;
   size_t o = kHeaderBytes;
-  f.off_cand_val = o; o = align256(o + cand * 4);
-  f.off_cand_id = o; o = align256(o + cand * 4);
+  f.off_cand = o; o = align256(o + cand * 8);
+  f.off_row_key = o; o = align256(o + (size_t)p.T * 4);
   f.off_unit_val = o; o = align256(o + unit * 4);
   f.off_unit_id = o; o = align256(o + unit * 4);
   f.total = o;
@@ -693,13 +707,15 @@ kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const u
   ep.col0 = 0;
   ep.cols = V;
   ep.topk_cap = f.cap;
-  ep.cand_val = at<float>(workspace, f.off_cand_val);
-  ep.cand_id = at<int32_t>(workspace, f.off_cand_id);
+  ep.cand = at<float2>(workspace, f.off_cand);
+  ep.row_key = at<uint32_t>(workspace, f.off_row_key);
+  KD_CUDA(cudaMemsetAsync(ep.row_key, 0, (size_t)T * 4, stream));
   ep.unit_val = at<float>(workspace, f.off_unit_val);
   ep.unit_id = at<int32_t>(workspace, f.off_unit_id);
   if (log_plan()) print_plan("topk", pair, procs, sh, f.grid);
   KD_CUDA(launch_gemm(GEMM_TOPK, LOGIT_BN, pair, tmH, tmW, sh, ep, status, f.grid, stream));
-  KD_CUDA(launch_topk_merge(ep.unit_val, ep.unit_id, f.nsplit, T, K, topk_idx, topk_logit, stream));
+  KD_CUDA(launch_topk_merge(ep.unit_val, ep.unit_id, ep.row_key, f.nsplit, T, K, topk_idx,
+                            topk_logit, stream));
   return KD_OK;
 }
 

@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "kdkl_internal.h"
 #include "tc_primitives.cuh"
 
@@ -176,36 +178,65 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
 }
 
 // Merge each row's per-split top-K lists into the row's top-K, sorted by
-// (logit descending, id ascending). One block per row; the nsplit x K entries
-// are sorted as 64-bit keys (inverted order key of the logit, then the id) by
-// a block-wide bitonic sort in shared memory (p2 = next power of two >= nsplit*K).
+// (logit descending, id ascending). One warp per row. Entries below the
+// row's shared threshold key (the best K-th logit any split reached, which is
+// at most the row's true K-th logit) cannot be in the top-K and are dropped;
+// the survivors (at least K) are compacted in order and sorted as 64-bit keys
+// (inverted order key of the logit, then the id) by a warp bitonic sort in
+// shared memory.
 __device__ __forceinline__ uint32_t merge_order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// One warp per row; `rows_per_block` warps share the block's shared memory,
+// cap entries (a power of two >= nsplit * K) each.
 __global__ void __launch_bounds__(256)
     topk_merge_kernel(const float* __restrict__ unit_val, const int32_t* __restrict__ unit_id,
-                      int nsplit, int T, int K, int p2, int32_t* __restrict__ out_id,
-                      float* __restrict__ out_val) {
-  extern __shared__ unsigned long long mkeys[];
-  const int t = blockIdx.x;
+                      const uint32_t* __restrict__ row_key, int nsplit, int T, int K, int cap,
+                      int32_t* __restrict__ out_id, float* __restrict__ out_val) {
+  extern __shared__ unsigned long long mkeys_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;  // whole warp leaves together; no block-wide barrier below
+  unsigned long long* mkeys = mkeys_all + (size_t)warp * cap;
   const int n = nsplit * K;
-  for (int e = threadIdx.x; e < p2; e += blockDim.x) {
-    unsigned long long key = ~0ull;
-    if (e < n) {
-      const int s = e / K, k = e - (e / K) * K;
-      const long long o = ((long long)s * T + t) * K + k;
-      const float v = unit_val[o];
-      const int32_t id = unit_id[o];
-      key = ((unsigned long long)(~merge_order_key(v)) << 32) | (uint32_t)id;
+  const uint32_t floor_key = row_key[t];
+  const uint32_t below = (1u << lane) - 1u;
+  int m = 0;
+  constexpr int BATCH = 8;  // independent loads in flight per lane
+  for (int e0 = 0; e0 < n; e0 += 32 * BATCH) {
+    float vb[BATCH];
+    int32_t ib[BATCH];
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const int e = e0 + b * 32 + lane;
+      if (e < n) {
+        const int s = e / K, k = e - s * K;
+        const long long o = ((long long)s * T + t) * K + k;
+        vb[b] = unit_val[o];
+        ib[b] = unit_id[o];
+      } else {
+        vb[b] = -INFINITY;
+        ib[b] = -1;
+      }
     }
-    mkeys[e] = key;
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const uint32_t ok = merge_order_key(vb[b]);
+      const bool keep = ib[b] >= 0 && ok >= floor_key;
+      const uint32_t mask = __ballot_sync(0xffffffffu, keep);
+      if (keep) mkeys[m + __popc(mask & below)] = ((unsigned long long)(~ok) << 32) | (uint32_t)ib[b];
+      m += __popc(mask);
+    }
   }
-  __syncthreads();
+  int p2 = 2;
+  while (p2 < m) p2 <<= 1;
+  for (int e = m + lane; e < p2; e += 32) mkeys[e] = ~0ull;
+  __syncwarp();
   for (int size = 2; size <= p2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (p2 >> 1); i += blockDim.x) {
+      for (int i = lane; i < (p2 >> 1); i += 32) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool ascending = (lo & size) == 0;
@@ -215,10 +246,10 @@ __global__ void __launch_bounds__(256)
           mkeys[hi] = a;
         }
       }
-      __syncthreads();
+      __syncwarp();
     }
   }
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+  for (int k = lane; k < K; k += 32) {
     const unsigned long long key = mkeys[k];
     const uint32_t ok = ~(uint32_t)(key >> 32);
     out_val[(long long)t * K + k] = __uint_as_float((ok & 0x80000000u) ? (ok & 0x7fffffffu) : ~ok);
@@ -264,12 +295,14 @@ int topk_merge_p2(int nsplit, int K) {
   return p2 < 2 ? 2 : p2;
 }
 
-cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, int nsplit, int T, int K,
-                              int32_t* out_id, float* out_val, cudaStream_t stream) {
-  const int p2 = topk_merge_p2(nsplit, K);
-  return launch_kernel("topk_merge", topk_merge_kernel, dim3(T), dim3(256),
-                       (size_t)p2 * sizeof(unsigned long long), stream, unit_val, unit_id, nsplit,
-                       T, K, p2, out_id, out_val);
+cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const uint32_t* row_key,
+                              int nsplit, int T, int K, int32_t* out_id, float* out_val,
+                              cudaStream_t stream) {
+  const int cap = topk_merge_p2(nsplit, K);  // <= 4096 entries, 32 KB per warp
+  const int warps = std::max(1, std::min(8, 6144 / cap));  // <= 48 KB of shared memory
+  return launch_kernel("topk_merge", topk_merge_kernel, dim3((T + warps - 1) / warps),
+                       dim3(32 * warps), (size_t)warps * cap * sizeof(unsigned long long), stream,
+                       unit_val, unit_id, row_key, nsplit, T, K, cap, out_id, out_val);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,

@@ -107,8 +107,8 @@ struct EpiParams {
   int accumulate;
   // EPI_TOPK (K is the field above)
   int topk_cap;      // capacity of a row's candidate list (K + 256, at most 512)
-  float* cand_val;   // [gridDim.x * BM, topk_cap] candidate logits, one list per (CTA, row)
-  int32_t* cand_id;  // same shape, vocabulary ids
+  float2* cand;      // [gridDim.x * BM, topk_cap] (logit, id bits), one list per (CTA, row)
+  uint32_t* row_key; // [T] order key of the best K-th logit any split has seen (0 = none)
   float* unit_val;   // [nsplit, T, K] each split's top-K per row (id order)
   int32_t* unit_id;
 };
@@ -127,20 +127,40 @@ __device__ __forceinline__ float f32_from_order_key(uint32_t k) {
 // ascending), in place and in the same id order. Returns the K-th best logit,
 // the row's new admission threshold: a later candidate of the same row has a
 // larger id, so only a strictly larger logit can displace a kept entry.
-// The K-th largest key is found by bisection over the 32-bit order keys.
-static __device__ __noinline__ float topk_compact_row(float* vals, int32_t* ids, int n, int K) {
+// The K-th largest key is found by bisection over the 32-bit order keys,
+// starting from the list's min/max keys and stopping early once a midpoint
+// separates exactly K keys.
+static __device__ __noinline__ float topk_compact_row(float2* list, int n, int K) {
   constexpr int MAXE = 16;  // 512 entries / 32 lanes
   const int lane = threadIdx.x & 31;
   __syncwarp();
   uint32_t key[MAXE];
-  int32_t idv[MAXE];
+  float idv[MAXE];  // id bits carried as a float
 #pragma unroll
   for (int i = 0; i < MAXE; ++i) {
     const int e = i * 32 + lane;
-    key[i] = e < n ? f32_order_key(vals[e]) : 0u;
-    idv[i] = e < n ? ids[e] : -1;
+    const float2 c = e < n ? list[e] : make_float2(0.f, 0.f);
+    key[i] = e < n ? f32_order_key(c.x) : 0u;
+    idv[i] = c.y;
   }
-  uint32_t lo = 0u, hi = 0xffffffffu;
+  // Search range: the list's own smallest and largest keys.
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int i = 0; i < MAXE; ++i) {
+    if (i * 32 + lane < n) {
+      lo = min(lo, key[i]);
+      hi = max(hi, key[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  // Invariant: at least K keys are >= lo. Stop early when a midpoint has
+  // exactly K keys at or above it (then those K are the top K and the
+  // threshold is the smallest of them); otherwise lo ends at the K-th key.
+  bool exact = false;
   while (lo < hi) {
     const uint32_t mid = lo + ((hi - lo) >> 1) + 1u;
     int c = 0;
@@ -148,7 +168,22 @@ static __device__ __noinline__ float topk_compact_row(float* vals, int32_t* ids,
     for (int i = 0; i < MAXE; ++i) c += (i * 32 + lane < n && key[i] >= mid) ? 1 : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (c >= K) lo = mid; else hi = mid - 1u;
+    if (c == K) {
+      lo = mid;
+      exact = true;
+      break;
+    }
+    if (c > K) lo = mid; else hi = mid - 1u;
+  }
+  if (exact) {
+    // the K kept keys are those >= lo; the threshold is the smallest of them
+    uint32_t kmin = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i)
+      if (i * 32 + lane < n && key[i] >= lo) kmin = min(kmin, key[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    lo = kmin;  // exactly K keys are >= kmin (no key lies in [kmin, mid) beyond those)
   }
   int gt = 0;
 #pragma unroll
@@ -168,16 +203,20 @@ static __device__ __noinline__ float topk_compact_row(float* vals, int32_t* ids,
     const int eq_rank = eq_seen + __popc(eq_mask & below);
     const bool keep = is_gt || (is_eq && eq_rank < need_eq);
     const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int pos = written + __popc(keep_mask & below);
-      vals[pos] = f32_from_order_key(key[i]);
-      ids[pos] = idv[i];
-    }
+    if (keep) list[written + __popc(keep_mask & below)] = make_float2(f32_from_order_key(key[i]), idv[i]);
     written += __popc(keep_mask);
     eq_seen += __popc(eq_mask);
   }
   __syncwarp();
   return f32_from_order_key(lo);
+}
+
+// Admission threshold from the best K-th logit published by any split of the
+// row: values equal to it are still admitted (an equal logit with a smaller
+// id may belong to the row's top-K), values below cannot be in the top-K.
+__device__ __forceinline__ float topk_shared_threshold(const uint32_t* row_key) {
+  const uint32_t k = *reinterpret_cast<const volatile uint32_t*>(row_key);
+  return k == 0u ? -INFINITY : nextafterf(f32_from_order_key(k), -INFINITY);
 }
 
 __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
@@ -425,14 +464,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // EPI_TOPK row state: admission threshold and candidate count
       float th = INFINITY;
       int cnt = 0;
-      float* c_val = nullptr;
-      int32_t* c_id = nullptr;
+      float2* c_list = nullptr;
+      uint32_t* rkey = nullptr;
       if (EPI == EPI_TOPK) {
         row_ok = r < ep.rows;
-        th = row_ok ? -INFINITY : INFINITY;
-        const long long slot = ((long long)blockIdx.x * BM + r_in_tile) * ep.topk_cap;
-        c_val = ep.cand_val + slot;
-        c_id = ep.cand_id + slot;
+        c_list = ep.cand + ((long long)blockIdx.x * BM + r_in_tile) * ep.topk_cap;
+        if (row_ok) {
+          rkey = ep.row_key + ep.row0 + r;
+          th = topk_shared_threshold(rkey);
+        }
       }
       if (EPI == EPI_LSE || EPI == EPI_GRAD) {
         row_ok = r < ep.rows;
@@ -475,12 +515,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               need &= need - 1u;
               const int ni = __shfl_sync(0xffffffffu, cnt, i);
               const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
-              const float thi = topk_compact_row(ep.cand_val + slot_i, ep.cand_id + slot_i, ni, ep.K);
+              const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
               if (lane == i) {
-                th = thi;
+                th = fmaxf(th, thi);
                 cnt = ep.K;
+                atomicMax(rkey, f32_order_key(thi));  // share with the row's other splits
               }
             }
+            if (c == 0 && row_ok) th = fmaxf(th, topk_shared_threshold(rkey));
           }
           float v[32];
           __syncwarp();
@@ -544,8 +586,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (j < nv && v[j] > th) {
-                c_val[cnt] = v[j];
-                c_id[cnt] = vid0 + j;
+                c_list[cnt] = make_float2(v[j], __int_as_float(vid0 + j));
                 ++cnt;
               }
             }
@@ -589,14 +630,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           need &= need - 1u;
           const int ni = __shfl_sync(0xffffffffu, cnt, i);
           const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
-          topk_compact_row(ep.cand_val + slot_i, ep.cand_id + slot_i, ni, ep.K);
-          if (lane == i) cnt = ep.K;
+          const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
+          if (lane == i) {
+            cnt = ep.K;
+            atomicMax(rkey, f32_order_key(thi));
+          }
         }
         if (row_ok) {
           const long long o = ((long long)s * ep.T + ep.row0 + r) * ep.K;
           for (int k = 0; k < ep.K; ++k) {
-            ep.unit_val[o + k] = k < cnt ? c_val[k] : -INFINITY;
-            ep.unit_id[o + k] = k < cnt ? c_id[k] : -1;
+            const float2 c = k < cnt ? c_list[k] : make_float2(-INFINITY, __int_as_float(-1));
+            ep.unit_val[o + k] = c.x;
+            ep.unit_id[o + k] = __float_as_int(c.y);
           }
         }
       }

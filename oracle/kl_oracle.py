@@ -226,3 +226,48 @@ def topk_logits(H, W, K: int):
         order = np.lexsort((np.arange(V), -z[t]))
         ids[t] = order[:K]
     return ids, np.take_along_axis(z, ids, axis=1)
+
+
+# --------------------------------------------------------------------------
+# Loss variant: the soft KL term mixed with a hard-label cross-entropy.
+# The pages report ablations over the choice of loss without printing one;
+# this is the standard distillation mix, read plainly:
+#   loss_t = alpha * c * KL_t(tau) + (1 - alpha) * CE_t,
+#   CE_t   = logsumexp_v z_{t,v} - z_{t, y_t}          (temperature 1),
+#   c      = tau^2 when scale_tau_sq else 1.
+# dL/dz = m_t / N * [alpha c (q_tau - P) / tau + (1 - alpha) (q_1 - onehot(y_t))].
+
+def forward_mixed(H, W, topk_idx, topk_logit, mask, tau: float, alpha: float,
+                  scale_tau_sq: bool, labels):
+    """Returns (loss, lse_tau [T], lse_1 [T], token_loss [T])."""
+    check_indices(topk_idx, np.asarray(W).shape[0])
+    check_indices(np.asarray(labels)[:, None], np.asarray(W).shape[0])
+    logq, lse = student_log_softmax(H, W, tau)
+    kl = token_kl(logq, topk_idx, teacher_probs(topk_logit, tau))
+    logq1, lse1 = student_log_softmax(H, W, 1.0)
+    ce = -np.take_along_axis(logq1, np.asarray(labels, dtype=np.int64)[:, None], axis=1)[:, 0]
+    c = tau * tau if scale_tau_sq else 1.0
+    tok = alpha * c * kl + (1.0 - alpha) * ce
+    m = np.asarray(mask) != 0
+    n = int(np.count_nonzero(m))
+    loss = float(np.sum(tok[m]) / n) if n else 0.0
+    return loss, lse, lse1, tok
+
+
+def backward_mixed(H, W, topk_idx, topk_logit, mask, tau: float, alpha: float,
+                   scale_tau_sq: bool, labels, grad_loss: float = 1.0):
+    """Returns (dH, dW) of grad_loss * forward_mixed's loss."""
+    V = np.asarray(W).shape[0]
+    logq, _ = student_log_softmax(H, W, tau)
+    P = dense_teacher(topk_idx, teacher_probs(topk_logit, tau), V)
+    logq1, _ = student_log_softmax(H, W, 1.0)
+    Y = np.zeros_like(logq1)
+    Y[np.arange(Y.shape[0]), np.asarray(labels, dtype=np.int64)] = 1.0
+    c = tau * tau if scale_tau_sq else 1.0
+    m = (np.asarray(mask) != 0).astype(np.float64)
+    n = mask_count(mask)
+    if n == 0:
+        return np.zeros_like(np.asarray(H, dtype=np.float64)), np.zeros_like(np.asarray(W, dtype=np.float64))
+    G = (alpha * c * (np.exp(logq) - P) / tau + (1.0 - alpha) * (np.exp(logq1) - Y))
+    G = G * (grad_loss * m / n)[:, None]
+    return G @ np.asarray(W, dtype=np.float64), G.T @ np.asarray(H, dtype=np.float64)

@@ -71,7 +71,8 @@ typedef struct {
                          fewer tokens x more vocabulary; results are the same) */
 } kd_kl_problem;
 
-/* Workspace bytes for kd_kl_forward (which = 0) or kd_kl_backward (which = 1).
+/* Workspace bytes for kd_kl_forward (which = 0), kd_kl_backward (which = 1),
+ * kd_kl_forward_ex (which = 2) or kd_kl_backward_ex (which = 3).
  * Linear in T (no T x V term). Returns 0 if the problem is invalid. */
 size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which);
 
@@ -104,6 +105,41 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
                          const float* lse, float grad_loss,
                          uint16_t* dH, float* dW, int accumulate_dW,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Loss variant. The pages report ablations over the choice of loss without
+ * printing one ("Making knowledge distillation cheap enough to run at scale",
+ * closing section); this is the standard distillation mix:
+ *   loss_t = alpha * c * KL_t(tau) + (1 - alpha) * CE_t,  c = tau^2 or 1,
+ *   CE_t   = log sum_v exp(z[t,v]) - z[t, labels[t]]      (temperature 1),
+ *   loss   = sum_t m[t] loss_t / N.
+ * dL/dz[t,v] = m[t]/N * (alpha c (softmax(z/tau) - P)/tau + (1-alpha)(softmax(z) - onehot)).
+ * Same kernels as the calls above, with the temperature-1 sum and the label
+ * logit added to the GEMM epilogues. */
+typedef struct {
+  float alpha;            /* weight of the soft term, in [0, 1]; 1 = KL only */
+  int32_t scale_tau_sq;   /* nonzero: the soft term and its gradient are scaled by tau^2 */
+  const int32_t* labels;  /* [T] device, hard labels in [0, V); may be NULL when alpha == 1 */
+} kd_kl_options;
+
+/* Workspace: kd_kl_workspace_size(prob, 2) for the forward, (prob, 3) for the backward.
+ *   lse        [T] fp32 out   logsumexp of z / tau
+ *   lse1       [T] fp32 out   logsumexp of z (temperature 1; equals lse when tau == 1)
+ *   token_loss [T] fp32 out or NULL   alpha c KL_t + (1 - alpha) CE_t before masking
+ * A label outside [0, V) is reported as KD_ERR_INDEX_RANGE by kd_kl_check_status. */
+kd_status kd_kl_forward_ex(const kd_kl_problem* prob, const kd_kl_options* opts,
+                           const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                           const float* topk_logit, const uint8_t* mask, float* loss, float* lse,
+                           float* lse1, float* token_loss, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Backward of grad_loss * loss. lse1 may be NULL when tau == 1 or alpha == 1. */
+kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts,
+                            const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                            const float* topk_logit, const uint8_t* mask, const float* lse,
+                            const float* lse1, float grad_loss, uint16_t* dH, float* dW,
+                            int accumulate_dW, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /* Allocation-free forward. The paper has no counterpart to this call; it
  * exists for callers that cannot allocate device memory for a workspace: code

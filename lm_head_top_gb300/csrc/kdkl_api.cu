@@ -192,7 +192,7 @@ SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d, int til
 struct FwdPlan {
   bool pair;
   int m_tiles, n_tiles, nsplit, group_n, grid;
-  size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_bsum, total;
+  size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_ps1, off_pzl, off_bsum, total;
 };
 
 struct BwdPlan {
@@ -214,7 +214,7 @@ bool problem_ok(const kd_kl_problem* p) {
   return true;
 }
 
-FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs) {
+FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, bool mix = false) {
   FwdPlan f{};
   const int tile_m = pair ? 2 * BM : BM;
   f.pair = pair;
@@ -232,6 +232,8 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs) 
   f.off_pm = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
   f.off_ps = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
   f.off_pd = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
+  f.off_ps1 = o; o = align256(o + (mix ? (size_t)f.nsplit * p.T * 4 : 0));
+  f.off_pzl = o; o = align256(o + (mix ? (size_t)f.nsplit * p.T * 4 : 0));
   f.off_bsum = o; o = align256(o + (size_t)combine_blocks((int)std::max<int64_t>(p.T, 1)) * 8);
   f.total = o;
   return f;
@@ -403,19 +405,36 @@ int64_t kd_launch_count(void) { return g_launches.load(); }
 
 size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which) {
   if (!problem_ok(prob)) return 0;
-  if (which == 0) {
+  if (which == 0 || which == 2) {
+    const bool mix = which == 2;
     DeviceInfo di;
     const int sms = (device_info(&di) == KD_OK) ? di.num_sms : 148;
     // The split count depends on the SM count and the tiling mode; size for
     // the larger of the two modes so the answer holds for either.
     // Pair plans are sized for any number of co-resident clusters up to sms/2.
-    size_t total = plan_forward(*prob, sms, false, sms).total;
+    size_t total = plan_forward(*prob, sms, false, sms, mix).total;
     for (int procs = 1; procs <= sms / 2; ++procs)
-      total = std::max(total, plan_forward(*prob, sms, true, procs).total);
+      total = std::max(total, plan_forward(*prob, sms, true, procs, mix).total);
     return total;
   }
-  if (which == 1) return plan_backward(*prob).total;
+  if (which == 1 || which == 3) return plan_backward(*prob).total;
   return 0;
+}
+
+struct MixWeights {
+  float kl, ce;  // per-token loss = kl * KL + ce * CE
+};
+
+static MixWeights mix_weights(const kd_kl_problem& p, const kd_kl_options& o) {
+  const float c = o.scale_tau_sq ? p.temperature * p.temperature : 1.0f;
+  return MixWeights{o.alpha * c, 1.0f - o.alpha};
+}
+
+static kd_status validate_options(const kd_kl_problem* prob, const kd_kl_options* o) {
+  if (!(o->alpha >= 0.0f && o->alpha <= 1.0f)) return KD_ERR_INVALID_ARG;
+  if (o->alpha < 1.0f && prob->T > 0 && !o->labels) return KD_ERR_INVALID_ARG;
+  if (!aligned(o->labels, 4)) return KD_ERR_ALIGNMENT;
+  return KD_OK;
 }
 
 static kd_status validate_common(const kd_kl_problem* prob, const void* H, const void* W,
@@ -436,20 +455,25 @@ static kd_status validate_common(const kd_kl_problem* prob, const void* H, const
   return KD_OK;
 }
 
-kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
-                        const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                        float* loss, float* lse, float* token_kl, void* workspace,
-                        size_t workspace_bytes, void* stream_ptr) {
+static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* opts,
+                              const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                              const float* topk_logit, const uint8_t* mask, float* loss, float* lse,
+                              float* lse1, float* token_kl, void* workspace,
+                              size_t workspace_bytes, void* stream_ptr) {
   kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
   if (st != KD_OK) return st;
   if (!loss || (prob->T > 0 && !lse)) return KD_ERR_INVALID_ARG;
   if (!aligned(loss, 4) || !aligned(lse, 4) || !aligned(token_kl, 4)) return KD_ERR_ALIGNMENT;
+  const bool mix = opts != nullptr;
+  if (mix && ((st = validate_options(prob, opts)) != KD_OK)) return st;
+  if (mix && prob->T > 0 && !lse1) return KD_ERR_INVALID_ARG;
+  if (!aligned(lse1, 4)) return KD_ERR_ALIGNMENT;
   DeviceInfo di;
   if ((st = device_info(&di)) != KD_OK) return st;
   if ((st = get_encoder()) != KD_OK) return st;
   const kd_kl_problem& p = *prob;
   const bool pair = use_pair();
-  const FwdPlan f = plan_forward(p, di.num_sms, pair, gemm_procs(di.num_sms, pair));
+  const FwdPlan f = plan_forward(p, di.num_sms, pair, gemm_procs(di.num_sms, pair), mix);
   if (workspace_bytes < f.total) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
@@ -467,8 +491,8 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   float* sp = at<float>(workspace, f.off_sp);
   float* ent = at<float>(workspace, f.off_ent);
 
-  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, T, K, V, inv_tau, sidx, sp, ent, n_count,
-                              status, stream));
+  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
+                              inv_tau, sidx, sp, ent, n_count, status, stream));
 
   CUtensorMap tmH, tmW;
   const int b_rows = f.pair ? LOGIT_BN / 2 : LOGIT_BN;  // W rows one CTA loads per tile
@@ -495,23 +519,61 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
   ep.pm = at<float>(workspace, f.off_pm);
   ep.ps = at<float>(workspace, f.off_ps);
   ep.pd = at<float>(workspace, f.off_pd);
+  if (mix) {
+    ep.labels = opts->labels;
+    ep.same_tau = p.temperature == 1.0f ? 1 : 0;
+    ep.ps1 = at<float>(workspace, f.off_ps1);
+    ep.pzl = at<float>(workspace, f.off_pzl);
+  }
   if (log_plan()) print_plan("fwd_lse", f.pair, gemm_procs(di.num_sms, f.pair), sh, f.grid);
-  KD_CUDA(launch_gemm(GEMM_FWD_LSE, LOGIT_BN, f.pair, tmH, tmW, sh, ep, status, f.grid, stream));
+  KD_CUDA(launch_gemm(mix ? GEMM_FWD_LSE_MIX : GEMM_FWD_LSE, LOGIT_BN, f.pair, tmH, tmW, sh, ep,
+                      status, f.grid, stream));
 
   double* bsum = at<double>(workspace, f.off_bsum);
-  KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, cl2, inv_tau, lse,
-                             token_kl, bsum, stream));
+  if (mix) {
+    const MixWeights mw = mix_weights(p, *opts);
+    KD_CUDA(launch_lse_combine_mix(ep.pm, ep.ps, ep.pd, ep.ps1, ep.pzl, f.nsplit, T, ent, mask, cl2,
+                                   inv_tau, mw.kl, mw.ce, lse, lse1, token_kl, bsum, stream));
+  } else {
+    KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, cl2, inv_tau, lse,
+                               token_kl, bsum, stream));
+  }
   KD_CUDA(launch_loss_finalize(bsum, combine_blocks(T), n_count, loss, stream));
   return KD_OK;
 }
 
-kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
-                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                         const float* lse, float grad_loss, uint16_t* dH, float* dW,
-                         int accumulate_dW, void* workspace, size_t workspace_bytes,
-                         void* stream_ptr) {
+kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                        const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                        float* loss, float* lse, float* token_kl, void* workspace,
+                        size_t workspace_bytes, void* stream_ptr) {
+  return forward_impl(prob, nullptr, H, W, topk_idx, topk_logit, mask, loss, lse, nullptr,
+                      token_kl, workspace, workspace_bytes, stream_ptr);
+}
+
+kd_status kd_kl_forward_ex(const kd_kl_problem* prob, const kd_kl_options* opts,
+                           const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                           const float* topk_logit, const uint8_t* mask, float* loss, float* lse,
+                           float* lse1, float* token_loss, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!opts) return KD_ERR_INVALID_ARG;
+  return forward_impl(prob, opts, H, W, topk_idx, topk_logit, mask, loss, lse, lse1, token_loss,
+                      workspace, workspace_bytes, stream);
+}
+
+static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* opts,
+                               const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                               const float* topk_logit, const uint8_t* mask, const float* lse,
+                               const float* lse1, float grad_loss, uint16_t* dH, float* dW,
+                               int accumulate_dW, void* workspace, size_t workspace_bytes,
+                               void* stream_ptr) {
   kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
   if (st != KD_OK) return st;
+  const bool mix = opts != nullptr;
+  if (mix && ((st = validate_options(prob, opts)) != KD_OK)) return st;
+  // temperature-1 logsumexp: needed when the CE term is on and tau != 1
+  if (mix && prob->T > 0 && !lse1 && opts->alpha < 1.0f && prob->temperature != 1.0f)
+    return KD_ERR_INVALID_ARG;
+  if (!aligned(lse1, 4)) return KD_ERR_ALIGNMENT;
   if (!dW || (prob->T > 0 && (!lse || !dH))) return KD_ERR_INVALID_ARG;
   if (!isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16) || !aligned(lse, 4)) return KD_ERR_ALIGNMENT;
@@ -538,8 +600,8 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
   uint16_t* Gbuf = at<uint16_t>(workspace, b.off_G);
   float* dH_acc = at<float>(workspace, b.off_dH);
 
-  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, T, K, V, inv_tau, sidx, sp, nullptr,
-                              n_count, status, stream));
+  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
+                              inv_tau, sidx, sp, nullptr, n_count, status, stream));
 
   const bool pair = use_pair();
   const int tile_m = pair ? 2 * BM : BM;
@@ -594,10 +656,18 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
         ep.g_over_tau = grad_loss * inv_tau;
         ep.G = Gbuf;
         ep.ldg = b.Vb_pad;
+        if (mix) {
+          const MixWeights mw = mix_weights(p, *opts);
+          ep.labels = opts->labels;
+          ep.same_tau = p.temperature == 1.0f ? 1 : 0;
+          ep.lse1 = lse1 ? lse1 : lse;
+          ep.kl_weight = grad_loss * mw.kl * inv_tau;
+          ep.ce_weight = grad_loss * mw.ce;
+        }
         const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
         if (log_plan() && vb == 0 && tb == 0) print_plan("bwd_grad", pair, procs, sh, grid);
-        KD_CUDA(launch_gemm(GEMM_BWD_GRAD, LOGIT_BN, pair, tmH_K, tmW_K, sh, ep, status, grid,
-                            stream));
+        KD_CUDA(launch_gemm(mix ? GEMM_BWD_GRAD_MIX : GEMM_BWD_GRAD, LOGIT_BN, pair, tmH_K, tmW_K,
+                            sh, ep, status, grid, stream));
       }
       // 2) dH[rows] (+)= G . W[cols]
       {
@@ -649,6 +719,26 @@ kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uin
   }
   KD_CUDA(launch_f32_to_bf16(dH_acc, dH, (long long)p.T * p.d, di.num_sms, stream));
   return KD_OK;
+}
+
+kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                         const float* lse, float grad_loss, uint16_t* dH, float* dW,
+                         int accumulate_dW, void* workspace, size_t workspace_bytes,
+                         void* stream_ptr) {
+  return backward_impl(prob, nullptr, H, W, topk_idx, topk_logit, mask, lse, nullptr, grad_loss, dH,
+                       dW, accumulate_dW, workspace, workspace_bytes, stream_ptr);
+}
+
+kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts,
+                            const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                            const float* topk_logit, const uint8_t* mask, const float* lse,
+                            const float* lse1, float grad_loss, uint16_t* dH, float* dW,
+                            int accumulate_dW, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!opts) return KD_ERR_INVALID_ARG;
+  return backward_impl(prob, opts, H, W, topk_idx, topk_logit, mask, lse, lse1, grad_loss, dH, dW,
+                       accumulate_dW, workspace, workspace_bytes, stream);
 }
 
 size_t kd_lmhead_topk_workspace_size(const kd_topk_problem* prob) {

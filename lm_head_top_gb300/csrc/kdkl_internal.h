@@ -54,14 +54,20 @@ cudaError_t launch_kernel_cluster(const char* name, void (*kern)(KArgs...), dim3
 }
 
 // kernels_small.cu
-cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
-                                int K, int V, float inv_tau, int32_t* sidx, float* sp, float* ent,
-                                int* n_count, int* status, cudaStream_t stream);
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
+                                const int32_t* labels, int T, int K, int V, float inv_tau,
+                                int32_t* sidx, float* sp, float* ent, int* n_count, int* status,
+                                cudaStream_t stream);
 int combine_blocks(int T);
 cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
                                const float* ent, const uint8_t* mask, float cl2, float inv_tau,
                                float* lse, float* token_kl, double* block_sums,
                                cudaStream_t stream);
+cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float* pd,
+                                   const float* ps1, const float* pzl, int nsplit, int T,
+                                   const float* ent, const uint8_t* mask, float cl2, float inv_tau,
+                                   float kl_w, float ce_w, float* lse, float* lse1,
+                                   float* token_loss, double* block_sums, cudaStream_t stream);
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,
                                  float* loss, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
@@ -78,7 +84,9 @@ enum GemmKind {
   GEMM_BWD_GRAD = 1,  // A = H (K-major), B = W (K-major), softmax - P into the bf16 buffer
   GEMM_DH = 2,        // A = G (K-major), B = W (MN-major), fp32 out
   GEMM_DW = 3,        // A = G (MN-major), B = H (MN-major), fp32 out
-  GEMM_TOPK = 4       // A = H (K-major), B = W (K-major), per-split top-K lists
+  GEMM_TOPK = 4,      // A = H (K-major), B = W (K-major), per-split top-K lists
+  GEMM_FWD_LSE_MIX = 5,   // forward with the temperature-1 sum and the label logit
+  GEMM_BWD_GRAD_MIX = 6   // backward gradient of the mixed soft + hard-label loss
 };
 // How many 2-CTA clusters of the GEMM kernel fit on the current device at once
 // (0 if unknown). The persistent grid must not exceed it.

@@ -86,6 +86,14 @@ cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA
       if (bn != LOGIT_BN) break;
       return launch_pick<EPI_GRAD, false, false, LOGIT_BN>(pair, "bwd_grad_gemm", tmA, tmB, sh,
                                                            ep, status, grid, stream);
+    case GEMM_FWD_LSE_MIX:
+      if (bn != LOGIT_BN) break;
+      return launch_pick<EPI_LSE_MIX, false, false, LOGIT_BN>(pair, "fwd_lse_mix_gemm", tmA, tmB,
+                                                              sh, ep, status, grid, stream);
+    case GEMM_BWD_GRAD_MIX:
+      if (bn != LOGIT_BN) break;
+      return launch_pick<EPI_GRAD_MIX, false, false, LOGIT_BN>(pair, "bwd_grad_mix_gemm", tmA,
+                                                               tmB, sh, ep, status, grid, stream);
     case GEMM_TOPK:
       if (bn != LOGIT_BN) break;
       return launch_pick<EPI_TOPK, false, false, LOGIT_BN>(pair, "topk_gemm", tmA, tmB, sh, ep,

@@ -26,9 +26,10 @@ constexpr int PREP_WARPS = 8;
 // One warp per token row. Dynamic shared memory: PREP_WARPS * p2 * 8 bytes.
 __global__ void __launch_bounds__(PREP_WARPS * 32)
     teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logit,
-                        const uint8_t* __restrict__ mask, int T, int K, int p2, int V, float inv_tau,
-                        int32_t* __restrict__ sidx, float* __restrict__ sp,
-                        float* __restrict__ ent, int* n_count, int* status) {
+                        const uint8_t* __restrict__ mask, const int32_t* __restrict__ labels,
+                        int T, int K, int p2, int V, float inv_tau, int32_t* __restrict__ sidx,
+                        float* __restrict__ sp, float* __restrict__ ent, int* n_count,
+                        int* status) {
   extern __shared__ uint8_t prep_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* keys = reinterpret_cast<int*>(prep_smem) + warp * p2;
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(PREP_WARPS * 32)
       po[k] = vals[k];
     }
     if (lane == 0) {
+      if (labels && (labels[t] < 0 || labels[t] >= V)) record_error(status, DEV_ERR_INDEX_RANGE);
       if (ent) ent[t] = h;
       if (mask == nullptr || mask[t] != 0) atomicAdd(&block_count, 1);
     }
@@ -140,6 +142,47 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     if (mask == nullptr || mask[t] != 0) contrib = (double)kl;
   }
   // fixed-shape tree reduction: deterministic
+  __shared__ double red[COMBINE_THREADS];
+  red[threadIdx.x] = contrib;
+  __syncthreads();
+  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) block_sums[blockIdx.x] = red[0];
+}
+
+// Mixed loss: per token alpha c KL + (1 - alpha) CE with CE = lse_1 - z_label.
+__global__ void __launch_bounds__(COMBINE_THREADS)
+    lse_combine_mix_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                           const float* __restrict__ pd, const float* __restrict__ ps1,
+                           const float* __restrict__ pzl, int nsplit, int T,
+                           const float* __restrict__ ent, const uint8_t* __restrict__ mask,
+                           float cl2, float inv_tau, float kl_w, float ce_w,
+                           float* __restrict__ lse, float* __restrict__ lse1,
+                           float* __restrict__ token_loss, double* __restrict__ block_sums) {
+  const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  if (t < T) {
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + t]);
+    float S = 0.f, S1 = 0.f, D = 0.f, Z = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const long long o = (long long)s * T + t;
+      S += ps[o] * exp2f((pm[o] - M) * cl2);
+      S1 += ps1[o] * exp2f((pm[o] - M) * 1.4426950408889634f);
+      D += pd[o];
+      Z += pzl[o];
+    }
+    const float l = M * inv_tau + logf(S);
+    const float l1 = M + logf(S1);
+    const float kl = ent[t] - D * inv_tau + l;
+    const float tok = kl_w * kl + ce_w * (l1 - Z);
+    lse[t] = l;
+    lse1[t] = l1;
+    if (token_loss) token_loss[t] = tok;
+    if (mask == nullptr || mask[t] != 0) contrib = (double)tok;
+  }
   __shared__ double red[COMBINE_THREADS];
   red[threadIdx.x] = contrib;
   __syncthreads();
@@ -259,17 +302,18 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------ host launchers
 
-cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask, int T,
-                                int K, int V, float inv_tau, int32_t* sidx, float* sp, float* ent,
-                                int* n_count, int* status, cudaStream_t stream) {
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
+                                const int32_t* labels, int T, int K, int V, float inv_tau,
+                                int32_t* sidx, float* sp, float* ent, int* n_count, int* status,
+                                cudaStream_t stream) {
   int p2 = 1;
   while (p2 < K) p2 <<= 1;
   if (p2 < 2) p2 = 2;
   const size_t smem = (size_t)PREP_WARPS * p2 * 8;
   const int blocks = (T + PREP_WARPS - 1) / PREP_WARPS;
   return launch_kernel("teacher_prep", teacher_prep_kernel, dim3(blocks), dim3(PREP_WARPS * 32),
-                       smem, stream, idx, logit, mask, T, K, p2, V, inv_tau, sidx, sp, ent,
-                       n_count, status);
+                       smem, stream, idx, logit, mask, labels, T, K, p2, V, inv_tau, sidx, sp,
+                       ent, n_count, status);
 }
 
 int combine_blocks(int T) { return (T + COMBINE_THREADS - 1) / COMBINE_THREADS; }
@@ -281,6 +325,16 @@ cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd
   return launch_kernel("lse_combine", lse_combine_kernel, dim3(combine_blocks(T)),
                        dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nsplit, T, ent, mask, cl2,
                        inv_tau, lse, token_kl, block_sums);
+}
+
+cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float* pd,
+                                   const float* ps1, const float* pzl, int nsplit, int T,
+                                   const float* ent, const uint8_t* mask, float cl2, float inv_tau,
+                                   float kl_w, float ce_w, float* lse, float* lse1,
+                                   float* token_loss, double* block_sums, cudaStream_t stream) {
+  return launch_kernel("lse_combine_mix", lse_combine_mix_kernel, dim3(combine_blocks(T)),
+                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, ps1, pzl, nsplit, T, ent,
+                       mask, cl2, inv_tau, kl_w, ce_w, lse, lse1, token_loss, block_sums);
 }
 
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,

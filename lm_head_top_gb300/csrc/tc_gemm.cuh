@@ -57,7 +57,7 @@ struct TileCfg {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 512;
 };
 
-enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2, EPI_TOPK = 3 };
+enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2, EPI_TOPK = 3, EPI_LSE_MIX = 4, EPI_GRAD_MIX = 5 };
 
 // Work decomposition: `units` = m_tiles * nsplit. A unit is one m-tile and one
 // split (a contiguous range of n-tiles). Units are numbered group by group:
@@ -105,6 +105,14 @@ struct EpiParams {
   int64_t ldo;
   int out_rows, out_cols;
   int accumulate;
+  // EPI_LSE_MIX / EPI_GRAD_MIX: soft KL mixed with a hard-label cross-entropy
+  const int32_t* labels;  // [T] hard label per token
+  int same_tau;           // tau == 1: the temperature-1 sums equal the tau sums
+  float* ps1;             // [nsplit, T] sum of exp2((z - max) * log2(e))   (LSE_MIX)
+  float* pzl;             // [nsplit, T] z at the label if in this split, else 0 (LSE_MIX)
+  const float* lse1;      // [T] logsumexp of z at temperature 1        (GRAD_MIX)
+  float kl_weight;        // alpha * c / tau (times g / N per counted row) (GRAD_MIX)
+  float ce_weight;        // (1 - alpha)     (times g / N per counted row) (GRAD_MIX)
   // EPI_TOPK (K is the field above)
   int topk_cap;      // capacity of a row's candidate list (K + 256, at most 512)
   float2* cand;      // [gridDim.x * BM, topk_cap] (logit, id bits), one list per (CTA, row)
@@ -246,6 +254,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmShape sh, const EpiParams ep, int* status) {
   using Cfg = TileCfg<BN, PAIR>;
+  constexpr bool IS_LSE = EPI == EPI_LSE || EPI == EPI_LSE_MIX;
+  constexpr bool IS_GRAD = EPI == EPI_GRAD || EPI == EPI_GRAD_MIX;
+  constexpr bool MIX = EPI == EPI_LSE_MIX || EPI == EPI_GRAD_MIX;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int B_STAGE_BYTES = Cfg::B_STAGE_BYTES;
   constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
@@ -474,7 +485,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           th = topk_shared_threshold(rkey);
         }
       }
-      if (EPI == EPI_LSE || EPI == EPI_GRAD) {
+      // MIX row state: temperature-1 sum, label logit, label id
+      float run_s1 = 0.f, zl = 0.f, lse12 = 0.f, w_kl = 0.f, w_ce = 0.f;
+      int lab = -1;
+      if (IS_LSE || IS_GRAD) {
         row_ok = r < ep.rows;
         if (row_ok) {
           const long long tok = (long long)ep.row0 + r;
@@ -482,12 +496,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           p_row = ep.sp + tok * ep.K;
           cursor = lower_bound_row(id_row, ep.K, ep.col0 + nb * BN);
           cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
-          if (EPI == EPI_GRAD) {
+          if (IS_GRAD) {
             lse2 = __ldg(ep.lse + tok) * 1.4426950408889634f;
             const int n = *ep.n_count;
             const bool counted = ep.mask == nullptr || __ldg(ep.mask + tok) != 0;
             scale = (counted && n > 0) ? ep.g_over_tau / (float)n : 0.f;
+            if (MIX) {
+              lse12 = __ldg(ep.lse1 + tok) * 1.4426950408889634f;
+              const float per_row = (counted && n > 0) ? 1.f / (float)n : 0.f;
+              w_kl = ep.kl_weight * per_row;  // kl_weight carries g * alpha * c / tau
+              w_ce = ep.ce_weight * per_row;  // ce_weight carries g * (1 - alpha)
+            }
           }
+          if (MIX) lab = ep.labels ? __ldg(ep.labels + tok) : -1;
         }
       }
       for (int n = nb; n < ne; ++n) {
@@ -502,7 +523,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           const int cl = n * BN + c * 32;  // column within this launch
-          if (EPI == EPI_LSE || EPI == EPI_GRAD || EPI == EPI_TOPK) {
+          if (IS_LSE || IS_GRAD || EPI == EPI_TOPK) {
             if (cl >= ep.cols) break;  // warp-uniform
           } else {
             if (cl >= ep.out_cols) break;
@@ -527,7 +548,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           float v[32];
           __syncwarp();
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
-          if (EPI == EPI_LSE) {
+          if (IS_LSE) {
             const int vid0 = ep.col0 + cl;
             if (cl + 32 > ep.cols) {
 #pragma unroll
@@ -543,7 +564,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc_s += ex2_approx(fmaf(v[j], ep.cl2, -nmc));
             run_sum = fmaf(run_sum, ex2_approx((run_max - nm) * ep.cl2), acc_s);
+            if (MIX && !ep.same_tau) {
+              constexpr float L2E = 1.4426950408889634f;
+              const float nm1 = nm * L2E;
+              float acc1 = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc1 += ex2_approx(fmaf(v[j], L2E, -nm1));
+              run_s1 = fmaf(run_s1, ex2_approx((run_max - nm) * L2E), acc1);
+            }
             run_max = nm;
+            if (MIX && row_ok && lab >= vid0 && lab < vid0 + 32 && lab < ep.col0 + ep.cols)
+              zl = select32(v, lab - vid0);
             if (row_ok) {
               const int vend = ep.col0 + min(cl + 32, ep.cols);
               while (cur_id < vend) {
@@ -552,16 +583,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
               }
             }
-          } else if (EPI == EPI_GRAD) {
+          } else if (IS_GRAD) {
             const int vid0 = ep.col0 + cl;
             float g[32];
+            if (MIX) {
+              // w_kl (q_tau - P) + w_ce (q_1 - onehot(label)); the weights hold m g / N
+              constexpr float L2E = 1.4426950408889634f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) g[j] = ex2_approx(fmaf(v[j], ep.cl2, -lse2));
+              for (int j = 0; j < 32; ++j) {
+                const float qt = ex2_approx(fmaf(v[j], ep.cl2, -lse2));
+                const float q1 = ep.same_tau ? qt : ex2_approx(fmaf(v[j], L2E, -lse12));
+                g[j] = fmaf(qt, w_kl, q1 * w_ce);
+              }
+              if (row_ok && lab >= vid0 && lab < vid0 + 32) {
+                const int jl = lab - vid0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = (j == jl) ? g[j] - w_ce : g[j];
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) g[j] = ex2_approx(fmaf(v[j], ep.cl2, -lse2));
+            }
             if (row_ok) {
               const int vend = ep.col0 + min(cl + 32, ep.cols);
               while (cur_id < vend) {
                 if (cur_id >= vid0) {
-                  const float pk = __ldg(p_row + cursor);
+                  const float pk = MIX ? __ldg(p_row + cursor) * w_kl : __ldg(p_row + cursor);
                   const int jj = cur_id - vid0;
 #pragma unroll
                   for (int j = 0; j < 32; ++j) g[j] = (j == jj) ? g[j] - pk : g[j];
@@ -569,6 +616,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ++cursor;
                 cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
               }
+              if (MIX) scale = 1.f;  // weights already applied
               uint4* dst = reinterpret_cast<uint4*>(ep.G + (long long)r * ep.ldg + cl);
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -645,11 +693,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      if (EPI == EPI_LSE && row_ok) {
+      if (IS_LSE && row_ok) {
         const long long o = (long long)s * ep.T + ep.row0 + r;
         ep.pm[o] = run_max;
         ep.ps[o] = run_sum;
         ep.pd[o] = dot;
+        if (MIX) {
+          ep.ps1[o] = ep.same_tau ? run_sum : run_s1;
+          ep.pzl[o] = zl;
+        }
       }
     }
   }

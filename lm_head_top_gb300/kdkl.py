@@ -36,6 +36,11 @@ class kd_kl_problem(ctypes.Structure):
                 ("K", ctypes.c_int32), ("temperature", ctypes.c_float), ("chunk", ctypes.c_int64)]
 
 
+class kd_kl_options(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("scale_tau_sq", ctypes.c_int32),
+                ("labels", ctypes.c_void_p)]
+
+
 class kd_topk_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("V", ctypes.c_int64),
                 ("K", ctypes.c_int32), ("reserved", ctypes.c_int32)]
@@ -58,6 +63,13 @@ _SIGS = {
     "kd_kl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P,
                                       ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
                                       _P]),
+    "kd_kl_forward_ex": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), ctypes.POINTER(kd_kl_options),
+                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                        _P]),
+    "kd_kl_backward_ex": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem),
+                                         ctypes.POINTER(kd_kl_options), _P, _P, _P, _P, _P, _P, _P,
+                                         ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
+                                         _P]),
     "kd_kl_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
                                              _P, _P, _P, _P]),
     "kd_lmhead_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_topk_problem)]),
@@ -196,6 +208,70 @@ def kd_kl_backward(H, W, topk_idx, topk_logit, mask, lse, *, temperature=1.0, ch
                                _stream_ptr(stream))
     if rc != KD_OK:
         raise KDKLError(rc, "kd_kl_backward")
+    return dH, dW
+
+
+def _options(alpha, scale_tau_sq, labels):
+    if labels is not None:
+        _check(labels, "labels", torch.int32, (labels.shape[0],))
+    return kd_kl_options(float(alpha), 1 if scale_tau_sq else 0,
+                         None if labels is None else labels.data_ptr())
+
+
+def kd_kl_forward_ex(H, W, topk_idx, topk_logit, mask=None, labels=None, *, temperature=1.0,
+                     chunk=1024, alpha=1.0, scale_tau_sq=False, want_token_loss=False,
+                     workspace=None, stream=None):
+    """Mixed loss alpha*c*KL(tau) + (1-alpha)*CE(labels), c = tau^2 if scale_tau_sq.
+    Returns (loss [1], lse [T] at tau, lse1 [T] at temperature 1, token_loss or None)."""
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(topk_idx, "topk_idx", torch.int32, (T, K))
+    _check(topk_logit, "topk_logit", torch.float32, (T, K))
+    if mask is not None:
+        _check(mask, "mask", torch.uint8, (T,))
+    dev = H.device
+    p = _problem(T, d, V, K, temperature, chunk)
+    o = _options(alpha, scale_tau_sq, labels)
+    workspace = _workspace(p, 2, dev, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    lse1 = torch.empty(T, dtype=torch.float32, device=dev)
+    tok = torch.empty(T, dtype=torch.float32, device=dev) if want_token_loss else None
+    rc = load().kd_kl_forward_ex(ctypes.byref(p), ctypes.byref(o), _ptr(H), _ptr(W), _ptr(topk_idx),
+                                 _ptr(topk_logit), _ptr(mask), _ptr(loss), _ptr(lse), _ptr(lse1),
+                                 _ptr(tok), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_kl_forward_ex")
+    return loss, lse, lse1, tok
+
+
+def kd_kl_backward_ex(H, W, topk_idx, topk_logit, mask, labels, lse, lse1, *, temperature=1.0,
+                      chunk=1024, alpha=1.0, scale_tau_sq=False, grad_loss=1.0, dH=None, dW=None,
+                      accumulate_dW=False, workspace=None, stream=None):
+    """Backward of grad_loss * kd_kl_forward_ex's loss. Returns (dH bf16, dW fp32)."""
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(lse, "lse", torch.float32, (T,))
+    dev = H.device
+    p = _problem(T, d, V, K, temperature, chunk)
+    o = _options(alpha, scale_tau_sq, labels)
+    workspace = _workspace(p, 3, dev, workspace)
+    dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dH is None else dH
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    rc = load().kd_kl_backward_ex(ctypes.byref(p), ctypes.byref(o), _ptr(H), _ptr(W),
+                                  _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), _ptr(lse),
+                                  _ptr(lse1), float(grad_loss), _ptr(dH), _ptr(dW),
+                                  1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(),
+                                  _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_kl_backward_ex")
     return dH, dW
 
 

@@ -1,0 +1,83 @@
+"""Mixed loss (alpha * c * KL(tau) + (1 - alpha) * CE(hard label)) on the GPU
+against the fp64 oracle; alpha = 1 without tau^2 must match the plain KL path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.kl_oracle as ok
+from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+from tests._helpers import GRAD_REL_L2, LOSS_RTOL, LSE_ATOL, rel_l2, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kdkl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_top_gb300 import kdkl as m
+    m.load()
+    return m
+
+
+@pytest.mark.parametrize("tau,alpha,sq", [(1.0, 0.5, False), (2.0, 0.3, True), (2.0, 0.0, True),
+                                          (1.5, 1.0, True), (0.7, 0.8, False)])
+@pytest.mark.parametrize("shape", [(131, 72, 1000, 7, 50), (300, 128, 3000, 16, 100),
+                                   (700, 64, 300, 5, 200)])
+def test_mixed_loss_against_oracle(kdkl, tau, alpha, sq, shape):
+    T, d, V, K, chunk = shape
+    w = WORKLOADS["small"].with_(T=T, d=d, V=V, K=K, chunk=chunk, tau=tau,
+                                 seq_len=max(T // 2, 1), pad_frac=0.2)
+    x = make_inputs(w, seed=11)
+    y = torch.from_numpy(np.random.default_rng(5).integers(0, V, T).astype(np.int32))
+    g = {k: v.cuda() for k, v in x.items()}
+    yl = y.cuda()
+    loss, lse, lse1, tok = kdkl.kd_kl_forward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"],
+                                                 g["mask"], yl, temperature=tau, chunk=chunk,
+                                                 alpha=alpha, scale_tau_sq=sq, want_token_loss=True)
+    dH, dW = kdkl.kd_kl_backward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], yl,
+                                    lse, lse1, temperature=tau, chunk=chunk, alpha=alpha,
+                                    scale_tau_sq=sq, grad_loss=0.9)
+    torch.cuda.synchronize()
+    H, W, idx, logit, mask = to_oracle(x)
+    r_loss, r_lse, r_lse1, r_tok = ok.forward_mixed(H, W, idx, logit, mask, tau, alpha, sq, y.numpy())
+    r_dH, r_dW = ok.backward_mixed(H, W, idx, logit, mask, tau, alpha, sq, y.numpy(), 0.9)
+    assert abs(loss.item() - r_loss) <= LOSS_RTOL * abs(r_loss)
+    assert np.abs(lse.cpu().numpy() - r_lse).max() <= LSE_ATOL
+    assert np.abs(lse1.cpu().numpy() - r_lse1).max() <= LSE_ATOL
+    assert np.abs(tok.cpu().numpy() - r_tok).max() <= 1e-3 * max(1.0, np.abs(r_tok).max())
+    assert rel_l2(dH.float().cpu().numpy(), r_dH) <= GRAD_REL_L2
+    assert rel_l2(dW.cpu().numpy(), r_dW) <= GRAD_REL_L2
+
+
+def test_alpha_one_matches_plain_path(kdkl):
+    w = WORKLOADS["small"].with_(T=256, d=64, V=2000, K=10, chunk=64, tau=2.0)
+    x = make_inputs(w, seed=12)
+    g = {k: v.cuda() for k, v in x.items()}
+    a_loss, a_lse, _ = kdkl.kd_kl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                                          temperature=2.0, chunk=64)
+    b_loss, b_lse, b_lse1, _ = kdkl.kd_kl_forward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"],
+                                                     g["mask"], None, temperature=2.0, chunk=64,
+                                                     alpha=1.0)
+    a_dH, a_dW = kdkl.kd_kl_backward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                                     a_lse, temperature=2.0, chunk=64)
+    b_dH, b_dW = kdkl.kd_kl_backward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                                        None, b_lse, b_lse1, temperature=2.0, chunk=64, alpha=1.0)
+    torch.cuda.synchronize()
+    assert a_loss.item() == b_loss.item()
+    assert torch.equal(a_lse, b_lse)
+    assert rel_l2(b_dW.cpu().numpy(), a_dW.cpu().numpy()) < 1e-5
+    assert rel_l2(b_dH.float().cpu().numpy(), a_dH.float().cpu().numpy()) < 1e-2
+
+
+def test_label_out_of_range_is_reported(kdkl):
+    w = WORKLOADS["small"].with_(T=64, d=16, V=100, K=3, chunk=16)
+    x = make_inputs(w, seed=13)
+    g = {k: v.cuda() for k, v in x.items()}
+    y = torch.zeros(64, dtype=torch.int32, device="cuda")
+    y[10] = 100
+    ws = torch.empty(kdkl.kd_kl_workspace_size(64, 16, 100, 3, 1.0, 16, 2), dtype=torch.uint8,
+                     device="cuda")
+    kdkl.kd_kl_forward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], y,
+                          chunk=16, alpha=0.5, workspace=ws)
+    assert kdkl.kd_kl_check_status(ws) == 4

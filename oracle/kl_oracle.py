@@ -271,3 +271,58 @@ def backward_mixed(H, W, topk_idx, topk_logit, mask, tau: float, alpha: float,
     G = (alpha * c * (np.exp(logq) - P) / tau + (1.0 - alpha) * (np.exp(logq1) - Y))
     G = G * (grad_loss * m / n)[:, None]
     return G @ np.asarray(W, dtype=np.float64), G.T @ np.asarray(H, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Reverse KL restricted to the cached ids (a loss-choice variant): both the
+# student and the teacher are renormalised over the row's K cached entries;
+# entries whose teacher logit is -inf are outside the support and dropped.
+#   qt_k = softmax_k(z[t, idx_k] / tau),  p_k = softmax_k(topk_logit_k / tau)
+#   RKL_t = sum_k qt_k (log qt_k - log p_k),   loss = sum_t m_t RKL_t / N
+# d RKL_t / d z[t, idx_k] = qt_k (log qt_k - log p_k - RKL_t) / tau
+
+def _support_logsoftmax(a, keep):
+    a = np.where(keep, a, -np.inf)
+    amax = np.max(a, axis=1, keepdims=True)
+    lse = amax[:, 0] + np.log(np.sum(np.where(keep, np.exp(a - amax), 0.0), axis=1))
+    return np.where(keep, a - lse[:, None], -np.inf)
+
+
+def reverse_kl_forward(H, W, topk_idx, topk_logit, mask, tau: float):
+    """Returns (loss, token_rkl [T], z_at [T,K]) with z_at = z[t, idx_k]."""
+    check_indices(topk_idx, np.asarray(W).shape[0])
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    z_at = np.take_along_axis(student_logits(H, W), idx, axis=1)
+    logit = np.asarray(topk_logit, dtype=np.float64)
+    keep = np.isfinite(logit)
+    logqt = _support_logsoftmax(z_at / tau, keep)
+    logp = _support_logsoftmax(logit / tau, keep)
+    qt = np.where(keep, np.exp(logqt), 0.0)
+    with np.errstate(invalid="ignore"):  # -inf - -inf only in dropped entries
+        rkl = np.sum(np.where(keep, qt * (logqt - logp), 0.0), axis=1)
+    m = np.asarray(mask) != 0
+    n = int(np.count_nonzero(m))
+    return (float(np.sum(rkl[m]) / n) if n else 0.0), rkl, z_at
+
+
+def reverse_kl_backward(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss: float = 1.0):
+    """Returns (dH, dW) of grad_loss * reverse_kl_forward's loss."""
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    _, rkl, z_at = reverse_kl_forward(H, W, idx, topk_logit, mask, tau)
+    logit = np.asarray(topk_logit, dtype=np.float64)
+    keep = np.isfinite(logit)
+    logqt = _support_logsoftmax(z_at / tau, keep)
+    logp = _support_logsoftmax(logit / tau, keep)
+    qt = np.where(keep, np.exp(logqt), 0.0)
+    m = (np.asarray(mask) != 0).astype(np.float64)
+    n = mask_count(mask)
+    if n == 0:
+        return np.zeros_like(H), np.zeros_like(W)
+    with np.errstate(invalid="ignore"):  # -inf - -inf only in dropped entries
+        gk = np.where(keep, qt * (logqt - logp - rkl[:, None]), 0.0) / tau
+    gk = gk * (grad_loss * m / n)[:, None]                  # [T, K] gradient of z at the ids
+    G = np.zeros((H.shape[0], W.shape[0]))
+    np.add.at(G, (np.repeat(np.arange(H.shape[0]), idx.shape[1]), idx.ravel()), gk.ravel())
+    return G @ W, G.T @ H

@@ -168,6 +168,44 @@ kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, co
                                 void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Second loss variant: reverse KL restricted to the cached ids. The pages
+ * report ablations over the choice of loss without printing one ("Making
+ * knowledge distillation cheap enough to run at scale", closing section);
+ * this is the mode-seeking direction, taken over the same support as the
+ * teacher cache (entries whose teacher logit is not finite are dropped from
+ * both distributions):
+ *   qt[t,k]  = softmax_k(z[t,idx[t,k]] / tau)      student, renormalised over the ids
+ *   p[t,k]   = softmax_k(topk_logit[t,k] / tau)    teacher, as above
+ *   RKL[t]   = sum_k qt[t,k] (log qt[t,k] - log p[t,k])
+ *   loss     = sum_t m[t] RKL[t] / N              (0 when N = 0)
+ *   dL/dz[t,idx[t,k]] = m[t]/N * qt (log qt - log p - RKL[t]) / tau, 0 elsewhere
+ * Only the K cached logits of each token enter, so there is no vocabulary-wide
+ * contraction: one warp per token gathers its K rows of W (CUDA cores).
+ * The problem struct is kd_kl_problem; `chunk` is not used (any value >= 1).
+ * Both calls take a workspace of kd_rkl_workspace_size() bytes (linear in T). */
+size_t kd_rkl_workspace_size(const kd_kl_problem* prob);
+
+/*   loss       [1] fp32 out       sum_t m[t] RKL[t] / N
+ *   token_rkl  [T] fp32 out or NULL   RKL[t] before masking
+ * Other arguments and errors as kd_kl_forward. */
+kd_status kd_rkl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                         float* loss, float* token_rkl, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Gradients of grad_loss * loss; recomputes the K logits per token (no forward
+ * state is needed).
+ *   dH  [T, d] bf16 out   overwritten (fp32 sums inside; masked rows = 0)
+ *   dW  [V, d] fp32 out   overwritten, or added to when accumulate_dW != 0;
+ *                         only the cached ids' rows receive contributions, added
+ *                         with fp32 atomics in no fixed order, so dW is not
+ *                         bitwise reproducible from run to run. */
+kd_status kd_rkl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
+                          const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                          float grad_loss, uint16_t* dH, float* dW, int accumulate_dW,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Offline teacher cache producer: for every row t of H, the K largest logits
  * z[t,v] = H[t] . W[v] over the full vocabulary, with their ids. This is the
  * cache the loss above consumes ("Making knowledge distillation cheap enough

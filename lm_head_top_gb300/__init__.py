@@ -6,5 +6,5 @@ synthetic input generator.
 """
 from .kdkl import (KDKLError, kd_kl_backward, kd_kl_check_status, kd_kl_forward,  # noqa: F401
                    kd_kl_workspace_size, kd_launch_count, kd_lmhead_topk,
-                   kd_lmhead_topk_workspace_size, kd_status_string, kd_timing_begin,
-                   kd_timing_end)
+                   kd_lmhead_topk_workspace_size, kd_rkl_backward, kd_rkl_forward,
+                   kd_rkl_workspace_size, kd_status_string, kd_timing_begin, kd_timing_end)

@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libkdkl.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["kernels_gemm.cu", "kernels_small.cu", "kdkl_api.cu", "kdkl_noalloc.cu"]
+SOURCES = ["kernels_gemm.cu", "kernels_small.cu", "kernels_rkl.cu", "kdkl_api.cu",
+           "kdkl_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

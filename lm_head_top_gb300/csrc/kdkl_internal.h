@@ -78,6 +78,18 @@ cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, con
                               int nsplit, int T, int K, int32_t* out_id, float* out_val,
                               cudaStream_t stream);
 
+// kernels_rkl.cu — reverse KL over the cached ids (CUDA cores, one warp per token)
+int rkl_blocks(int T);
+cudaError_t launch_rkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* idx,
+                               const float* logit, const uint8_t* mask, int T, int d, int K, int V,
+                               float inv_tau, float* token_rkl, double* block_sums, int* n_count,
+                               int* status, cudaStream_t stream);
+// Counts the unmasked tokens into *n_count (zeroed by the caller), then the gradient.
+cudaError_t launch_rkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* idx,
+                                const float* logit, const uint8_t* mask, int T, int d, int K, int V,
+                                float inv_tau, float grad_loss, int* n_count, uint16_t* dH,
+                                float* dW, int* status, int num_sms, cudaStream_t stream);
+
 // kernels_gemm.cu — tcgen05 GEMMs (see tc_gemm.cuh for the epilogues)
 enum GemmKind {
   GEMM_FWD_LSE = 0,   // A = H (K-major), B = W (K-major), online logsumexp + gather

@@ -72,6 +72,12 @@ _SIGS = {
                                          _P]),
     "kd_kl_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
                                              _P, _P, _P, _P]),
+    "kd_rkl_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_kl_problem)]),
+    "kd_rkl_forward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P, _P,
+                                      _P, ctypes.c_size_t, _P]),
+    "kd_rkl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
+                                       ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
+                                       _P]),
     "kd_lmhead_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_topk_problem)]),
     "kd_lmhead_topk": (ctypes.c_int, [ctypes.POINTER(kd_topk_problem), _P, _P, _P, _P, _P,
                                       ctypes.c_size_t, _P]),
@@ -302,6 +308,66 @@ def kd_kl_forward_noalloc(H, W, topk_idx, topk_logit, mask=None, *, temperature=
     if rc != KD_OK:
         raise KDKLError(rc, "kd_kl_forward_noalloc")
     return loss, lse, token_kl
+
+
+def kd_rkl_workspace_size(T, d, V, K, temperature=1.0) -> int:
+    p = _problem(T, d, V, K, temperature, 1)
+    return int(load().kd_rkl_workspace_size(ctypes.byref(p)))
+
+
+def _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace):
+    T, d = H.shape
+    V = W.shape[0]
+    K = topk_idx.shape[1]
+    _check(H, "H", torch.bfloat16, (T, d))
+    _check(W, "W", torch.bfloat16, (V, d))
+    _check(topk_idx, "topk_idx", torch.int32, (T, K))
+    _check(topk_logit, "topk_logit", torch.float32, (T, K))
+    if mask is not None:
+        _check(mask, "mask", torch.uint8, (T,))
+    p = _problem(T, d, V, K, temperature, 1)
+    if workspace is None:
+        need = int(load().kd_rkl_workspace_size(ctypes.byref(p)))
+        if need == 0:
+            raise KDKLError(2, "kd_rkl_workspace_size")
+        workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+    return p, workspace
+
+
+def kd_rkl_forward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0,
+                   want_token_rkl=False, loss=None, token_rkl=None, workspace=None, stream=None):
+    """Reverse KL over the cached ids. Returns (loss [1] fp32, token_rkl [T] fp32 or None)."""
+    p, workspace = _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace)
+    dev = H.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    if want_token_rkl and token_rkl is None:
+        token_rkl = torch.empty(H.shape[0], dtype=torch.float32, device=dev)
+    rc = load().kd_rkl_forward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
+                               _ptr(topk_logit), _ptr(mask), _ptr(loss), _ptr(token_rkl),
+                               _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_rkl_forward")
+    return loss, token_rkl
+
+
+def kd_rkl_backward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0, grad_loss=1.0,
+                    dH=None, dW=None, accumulate_dW=False, workspace=None, stream=None):
+    """Backward of grad_loss * reverse-KL loss. Returns (dH [T,d] bf16, dW [V,d] fp32)."""
+    p, workspace = _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace)
+    dev = H.device
+    T, d = H.shape
+    dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dH is None else dH
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty((W.shape[0], d), dtype=torch.float32, device=dev)
+    rc = load().kd_rkl_backward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
+                                _ptr(topk_logit), _ptr(mask), float(grad_loss), _ptr(dH), _ptr(dW),
+                                1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
+    if rc != KD_OK:
+        raise KDKLError(rc, "kd_rkl_backward")
+    return dH, dW
 
 
 def kd_lmhead_topk_workspace_size(T, d, V, K) -> int:

@@ -117,3 +117,41 @@ def test_workspace_linear_in_T_no_TxV(lib, name):
     per_token = 2 * 4 * w.K + 4 * w.d  # sorted teacher (id, p) + fp32 dH accumulator
     g_budget = 2 * w.chunk * w.V * 1.07 + 2 * 256 * w.T + 2 * 128 * w.V
     assert bwd <= w.T * per_token + g_budget + (1 << 20)
+
+
+def _rkl_fwd(lib, p, H=16, ws=256, loss=64):
+    P = ctypes.c_void_p
+    return lib.kd_rkl_forward(ctypes.byref(p), P(H), P(16), P(16), P(16), None, P(loss), None,
+                              P(ws), 1 << 30, None)
+
+
+def _rkl_bwd(lib, p, dH=4096, dW=8192, g=1.0):
+    P = ctypes.c_void_p
+    return lib.kd_rkl_backward(ctypes.byref(p), P(16), P(16), P(16), P(16), None, g, P(dH), P(dW),
+                               0, P(256), 1 << 30, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d", 12, 3), ("d", 0, 2), ("K", 0, 2), ("K", 513, 2), ("K", 101, 2), ("T", -1, 2),
+    ("temperature", 0.0, 1), ("temperature", float("nan"), 1),
+])
+def test_rkl_argument_errors_are_synchronous(lib, field, value, code):
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 1)
+    setattr(p, field, value)
+    assert _rkl_fwd(lib, p) == code
+    assert _rkl_bwd(lib, p) == code
+    assert lib.kd_rkl_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_rkl_pointer_errors_and_workspace(lib):
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 1)
+    assert _rkl_fwd(lib, p, ws=0) == 5
+    assert _rkl_fwd(lib, p, H=0) == 1
+    assert _rkl_fwd(lib, p, loss=0) == 1
+    assert _rkl_fwd(lib, p, H=8) == 3
+    assert _rkl_bwd(lib, p, dW=0) == 1
+    assert _rkl_bwd(lib, p, dH=24) == 3
+    assert _rkl_bwd(lib, p, g=float("inf")) == 1
+    # header plus 8 bytes per 8 tokens: linear in T, independent of V and d
+    sizes = [kdkl.kd_rkl_workspace_size(T, 2880, 201088, 100) for T in (8192, 16384, 32768)]
+    assert sizes[0] < sizes[1] < sizes[2] <= 256 + 32768 + 256

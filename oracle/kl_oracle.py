@@ -305,10 +305,9 @@ def reverse_kl_forward(H, W, topk_idx, topk_logit, mask, tau: float):
     return (float(np.sum(rkl[m]) / n) if n else 0.0), rkl, z_at
 
 
-def reverse_kl_backward(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss: float = 1.0):
-    """Returns (dH, dW) of grad_loss * reverse_kl_forward's loss."""
-    H = np.asarray(H, dtype=np.float64)
-    W = np.asarray(W, dtype=np.float64)
+def reverse_kl_grad_z(H, W, topk_idx, topk_logit, mask, tau: float):
+    """[T,K] derivative of reverse_kl_forward's loss with respect to the
+    student logit z[t, idx_k] (0 for entries outside the support)."""
     idx = np.asarray(topk_idx, dtype=np.int64)
     _, rkl, z_at = reverse_kl_forward(H, W, idx, topk_logit, mask, tau)
     logit = np.asarray(topk_logit, dtype=np.float64)
@@ -319,10 +318,18 @@ def reverse_kl_backward(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss:
     m = (np.asarray(mask) != 0).astype(np.float64)
     n = mask_count(mask)
     if n == 0:
-        return np.zeros_like(H), np.zeros_like(W)
+        return np.zeros(idx.shape)
     with np.errstate(invalid="ignore"):  # -inf - -inf only in dropped entries
         gk = np.where(keep, qt * (logqt - logp - rkl[:, None]), 0.0) / tau
-    gk = gk * (grad_loss * m / n)[:, None]                  # [T, K] gradient of z at the ids
+    return gk * (m / n)[:, None]
+
+
+def reverse_kl_backward(H, W, topk_idx, topk_logit, mask, tau: float, grad_loss: float = 1.0):
+    """Returns (dH, dW) of grad_loss * reverse_kl_forward's loss."""
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    gk = grad_loss * reverse_kl_grad_z(H, W, idx, topk_logit, mask, tau)
     G = np.zeros((H.shape[0], W.shape[0]))
     np.add.at(G, (np.repeat(np.arange(H.shape[0]), idx.shape[1]), idx.ravel()), gk.ravel())
     return G @ W, G.T @ H

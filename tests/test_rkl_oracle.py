@@ -86,3 +86,26 @@ def test_finite_differences():
             num[i, j] = (ok.reverse_kl_forward(Hp, W, idx, logit, mask, 2.0)[0] -
                          ok.reverse_kl_forward(Hm, W, idx, logit, mask, 2.0)[0]) / (2 * h)
     assert np.linalg.norm(dH - num) / np.linalg.norm(num) < 1e-7
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.5])
+def test_grad_z_against_torch_autograd(tau):
+    """dloss/dz at the cached ids, taken by autograd with the gathered logits
+    as the leaf (masked tokens and -inf teacher entries included)."""
+    rng = np.random.default_rng(7)
+    T, d, V, K = 7, 6, 25, 6
+    H, W, idx, logit, mask = _rand_problem(rng, T, d, V, K)
+    logit[1, 2] = -np.inf
+    z = torch.tensor(np.take_along_axis(H @ W.T, idx, axis=1), requires_grad=True)
+    m = torch.tensor(mask != 0, dtype=torch.float64)
+    rows = []
+    for t in range(T):  # each row over its own support only
+        keep = torch.tensor(np.flatnonzero(np.isfinite(logit[t])))
+        logq = torch.log_softmax(z[t, keep] / tau, 0)
+        logp = torch.log_softmax(torch.tensor(logit[t])[keep] / tau, 0)
+        rows.append((logq.exp() * (logq - logp)).sum())
+    loss = (torch.stack(rows) * m).sum() / m.sum()
+    loss.backward()
+    gz = ok.reverse_kl_grad_z(H, W, idx, logit, mask, tau)
+    np.testing.assert_allclose(gz, z.grad.numpy(), rtol=1e-10, atol=1e-14)
+    assert np.all(gz[mask == 0] == 0.0) and gz[1, 2] == 0.0

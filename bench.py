@@ -409,6 +409,102 @@ def run_topk(args):
     }
 
 
+def run_rkl(args):
+    """Reverse KL over the cached ids (the loss-choice variant) on the same
+    workload: kd_rkl_forward + kd_rkl_backward per step."""
+    from lm_head_top_gb300 import kdkl
+    from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    kdkl.load()
+    w = WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_(T=args.tokens)
+    x = make_inputs(w, seed=rank, topk_device=dev)
+    T, d, V, K = w.T, w.d, w.V, w.K
+    torch.cuda.reset_peak_memory_stats(dev)
+    g = {k: v.to(dev) for k, v in x.items()}
+    ws = torch.empty(kdkl.kd_rkl_workspace_size(T, d, V, K, w.tau), dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    gz = torch.empty(T, K, dtype=torch.float32, device=dev)
+    dH = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                            temperature=w.tau, loss=loss, grad_z=gz, workspace=ws, stream=stream)
+        kdkl.kd_rkl_backward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                             temperature=w.tau, grad_z=gz, dH=dH, dW=dW, workspace=ws,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if kdkl.kd_kl_check_status(ws):
+        raise SystemExit("device status after warm-up: %s"
+                         % kdkl.kd_status_string(kdkl.kd_kl_check_status(ws)))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kdkl.kd_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        kdkl.kd_timing_begin()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_kernel = kdkl.kd_timing_end()
+        barrier(world)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    # Algorithmic bytes per launch of each large kernel: every distinct W row
+    # the cache names read once, H read once, the cache (ids, logits or the
+    # saved gradient) read once, outputs written once.
+    distinct = int(np.unique(x["topk_idx"].numpy()).size)
+    pairs = T * K
+    algo_bytes = {
+        "rkl_forward": distinct * d * 2 + T * d * 2 + pairs * 8 + T + pairs * 4,
+        "rkl_dH": distinct * d * 2 + pairs * 8 + T * d * 2,
+        "rkl_dW_segment": T * d * 2 + pairs * 12 + distinct * d * 4,
+    }
+    rows = {n: (c, ms) for n, c, ms in per_kernel}
+    dom = max(algo_bytes, key=lambda n: rows.get(n, (1, 0.0))[1])
+    c, ms = rows[dom]
+    algo = algo_bytes[dom]
+    achieved = algo / (ms / c / 1e3) / 1e9
+    # what the design streams: one row (W for rkl_forward and rkl_dH, H for the
+    # dW segments) of d bf16 per (token, id) pair, whatever the cache hits
+    gather_gbs = pairs * d * 2 / (ms / c / 1e3) / 1e9
+    return {
+        "metric": "reverse KL over the cached ids fwd+bwd tokens/s", "path": "rkl",
+        "value": round(T * world * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s_rkl" % w.name if not args.tokens else "%s_T%d_rkl" % (w.name, T),
+                   "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "distinct_ids": distinct,
+                   "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
+        "peak_hbm_gib": round(torch.cuda.max_memory_allocated(dev) / 2 ** 30, 3),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "peak_source": "%s hbm_gbs" % pk_src, "bytes_per_launch": algo,
+                     "pair_gather_gbs": round(gather_gbs, 1),
+                     "pair_gather_frac": round(gather_gbs / pk["hbm_gbs"], 4),
+                     "traffic": None},
+        "gpu_launches": kdkl.kd_launch_count() - launches0,
+        "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
+        "clocks": clocks.summary(),
+    }
+
+
 def run_reference(args):
     """The fp64 CPU oracle on bounded token samples of the same workload."""
     from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
@@ -446,8 +542,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("kdkl", "reference"), default="kdkl")
-    ap.add_argument("--path", choices=("kl", "topk"), default="kl",
-                    help="kl: fused KL fwd+bwd (the headline); topk: offline top-K cache producer")
+    ap.add_argument("--path", choices=("kl", "topk", "rkl"), default="kl",
+                    help="kl: fused KL fwd+bwd (the headline); topk: offline top-K cache "
+                         "producer; rkl: reverse KL over the cached ids")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -462,6 +559,8 @@ def main():
         res = run_reference(args)
     elif args.path == "topk":
         res = run_topk(args)
+    elif args.path == "rkl":
+        res = run_rkl(args)
     else:
         res = run_kdkl(args)
     if res is not None:

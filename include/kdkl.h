@@ -178,32 +178,40 @@ kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, co
  *   p[t,k]   = softmax_k(topk_logit[t,k] / tau)    teacher, as above
  *   RKL[t]   = sum_k qt[t,k] (log qt[t,k] - log p[t,k])
  *   loss     = sum_t m[t] RKL[t] / N              (0 when N = 0)
- *   dL/dz[t,idx[t,k]] = m[t]/N * qt (log qt - log p - RKL[t]) / tau, 0 elsewhere
+ *   grad_z[t,k] = dloss/dz[t,idx[t,k]] = m[t]/N * qt (log qt - log p - RKL[t]) / tau
+ *               (0 for dropped entries)
  * Only the K cached logits of each token enter, so there is no vocabulary-wide
- * contraction: one warp per token gathers its K rows of W (CUDA cores).
- * The problem struct is kd_kl_problem; `chunk` is not used (any value >= 1).
- * Both calls take a workspace of kd_rkl_workspace_size() bytes (linear in T). */
+ * contraction: the kernels gather rows of W (CUDA cores). The problem struct
+ * is kd_kl_problem; `chunk` is not used (any value >= 1); T * K < 2^31.
+ * Both calls take a workspace of kd_rkl_workspace_size() bytes: linear in T,
+ * plus 8 bytes per vocabulary row. */
 size_t kd_rkl_workspace_size(const kd_kl_problem* prob);
 
-/*   loss       [1] fp32 out       sum_t m[t] RKL[t] / N
+/*   loss       [1] fp32 out           sum_t m[t] RKL[t] / N
  *   token_rkl  [T] fp32 out or NULL   RKL[t] before masking
+ *   grad_z     [T, K] fp32 out or NULL   dloss/dz at the cached ids (upstream
+ *                                     gradient 1); passing it to kd_rkl_backward
+ *                                     saves the backward its logit recompute
  * Other arguments and errors as kd_kl_forward. */
 kd_status kd_rkl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                          const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                         float* loss, float* token_rkl, void* workspace, size_t workspace_bytes,
-                         void* stream);
+                         float* loss, float* token_rkl, float* grad_z, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
-/* Gradients of grad_loss * loss; recomputes the K logits per token (no forward
- * state is needed).
- *   dH  [T, d] bf16 out   overwritten (fp32 sums inside; masked rows = 0)
- *   dW  [V, d] fp32 out   overwritten, or added to when accumulate_dW != 0;
- *                         only the cached ids' rows receive contributions, added
- *                         with fp32 atomics in no fixed order, so dW is not
- *                         bitwise reproducible from run to run. */
+/* Gradients of grad_loss * loss.
+ *   grad_z  [T, K] fp32 or NULL   from kd_rkl_forward on the same inputs; NULL:
+ *                                 the backward recomputes it (one more gather of W)
+ *   dH      [T, d] bf16 out       overwritten (fp32 sums inside; masked rows = 0)
+ *   dW      [V, d] fp32 out       overwritten, or added to when accumulate_dW != 0
+ * The (id, token) pairs are sorted by id inside the call so that each dW row is
+ * summed by one warp in token order: no atomics, and both outputs are bitwise
+ * reproducible from run to run. An id outside [0, V) contributes nothing and is
+ * reported as KD_ERR_INDEX_RANGE by kd_kl_check_status. */
 kd_status kd_rkl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                           const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                          float grad_loss, uint16_t* dH, float* dW, int accumulate_dW,
-                          void* workspace, size_t workspace_bytes, void* stream);
+                          const float* grad_z, float grad_loss, uint16_t* dH, float* dW,
+                          int accumulate_dW, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* ---------------------------------------------------------------------------
  * Offline teacher cache producer: for every row t of H, the K largest logits

@@ -741,61 +741,75 @@ kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts
                        accumulate_dW, workspace, workspace_bytes, stream);
 }
 
+static bool rkl_problem_ok(const kd_kl_problem* p) {
+  return problem_ok(p) && p->T * (int64_t)p->K < (1ll << 31);
+}
+
 size_t kd_rkl_workspace_size(const kd_kl_problem* prob) {
-  if (!problem_ok(prob)) return 0;
-  // header, then one fp64 partial sum per forward block
-  return kHeaderBytes + align256((size_t)rkl_blocks((int)prob->T) * sizeof(double));
+  if (!rkl_problem_ok(prob)) return 0;
+  return rkl_layout(prob->T, prob->d, prob->K, prob->V, kHeaderBytes).total;
+}
+
+static kd_status rkl_validate(const kd_kl_problem* prob, const void* H, const void* W,
+                              const void* idx, const void* logit, const void* workspace,
+                              size_t workspace_bytes, const void* grad_z) {
+  kd_status st = validate_common(prob, H, W, idx, logit, workspace);
+  if (st != KD_OK) return st;
+  if (prob->T * (int64_t)prob->K >= (1ll << 31)) return KD_ERR_SHAPE;
+  if (!aligned(grad_z, 4)) return KD_ERR_ALIGNMENT;
+  if (workspace_bytes < kd_rkl_workspace_size(prob)) return KD_ERR_WORKSPACE;
+  return KD_OK;
 }
 
 kd_status kd_rkl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                          const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                         float* loss, float* token_rkl, void* workspace, size_t workspace_bytes,
-                         void* stream_ptr) {
-  kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
+                         float* loss, float* token_rkl, float* grad_z, void* workspace,
+                         size_t workspace_bytes, void* stream_ptr) {
+  kd_status st =
+      rkl_validate(prob, H, W, topk_idx, topk_logit, workspace, workspace_bytes, grad_z);
   if (st != KD_OK) return st;
   if (!loss) return KD_ERR_INVALID_ARG;
   if (!aligned(loss, 4) || !aligned(token_rkl, 4)) return KD_ERR_ALIGNMENT;
   DeviceInfo di;
   if ((st = device_info(&di)) != KD_OK) return st;
-  if (workspace_bytes < kd_rkl_workspace_size(prob)) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int* status = at<int>(workspace, 0);
-  int* n_count = status + 1;
   KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
   if (prob->T == 0) {
     KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
     return KD_OK;
   }
-  const int T = (int)prob->T;
-  double* bsum = at<double>(workspace, kHeaderBytes);
-  KD_CUDA(launch_rkl_forward(H, W, topk_idx, topk_logit, mask, T, (int)prob->d, prob->K,
-                             (int)prob->V, 1.0f / prob->temperature, token_rkl, bsum, n_count,
-                             status, stream));
-  KD_CUDA(launch_loss_finalize(bsum, rkl_blocks(T), n_count, loss, stream));
+  const RklLayout L = rkl_layout(prob->T, prob->d, prob->K, prob->V, kHeaderBytes);
+  KD_CUDA(rkl_forward(L, H, W, topk_idx, topk_logit, mask, (int)prob->T, (int)prob->d, prob->K,
+                      (int)prob->V, 1.0f / prob->temperature, token_rkl, grad_z, loss, workspace,
+                      status, status + 1, di.num_sms, stream));
   return KD_OK;
 }
 
 kd_status kd_rkl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                           const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
-                          float grad_loss, uint16_t* dH, float* dW, int accumulate_dW,
-                          void* workspace, size_t workspace_bytes, void* stream_ptr) {
-  kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
+                          const float* grad_z, float grad_loss, uint16_t* dH, float* dW,
+                          int accumulate_dW, void* workspace, size_t workspace_bytes,
+                          void* stream_ptr) {
+  kd_status st =
+      rkl_validate(prob, H, W, topk_idx, topk_logit, workspace, workspace_bytes, grad_z);
   if (st != KD_OK) return st;
   if (!dW || (prob->T > 0 && !dH)) return KD_ERR_INVALID_ARG;
   if (!isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_ALIGNMENT;
   DeviceInfo di;
   if ((st = device_info(&di)) != KD_OK) return st;
-  if (workspace_bytes < kd_rkl_workspace_size(prob)) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int* status = at<int>(workspace, 0);
-  int* n_count = status + 1;
   KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
-  if (!accumulate_dW) KD_CUDA(cudaMemsetAsync(dW, 0, (size_t)prob->V * prob->d * 4, stream));
-  if (prob->T == 0) return KD_OK;
-  KD_CUDA(launch_rkl_backward(H, W, topk_idx, topk_logit, mask, (int)prob->T, (int)prob->d,
-                              prob->K, (int)prob->V, 1.0f / prob->temperature, grad_loss, n_count,
-                              dH, dW, status, di.num_sms, stream));
+  if (prob->T == 0) {
+    if (!accumulate_dW) KD_CUDA(cudaMemsetAsync(dW, 0, (size_t)prob->V * prob->d * 4, stream));
+    return KD_OK;
+  }
+  const RklLayout L = rkl_layout(prob->T, prob->d, prob->K, prob->V, kHeaderBytes);
+  KD_CUDA(rkl_backward(L, H, W, topk_idx, topk_logit, mask, (int)prob->T, (int)prob->d, prob->K,
+                       (int)prob->V, 1.0f / prob->temperature, grad_z, grad_loss, dH, dW,
+                       accumulate_dW ? 1 : 0, workspace, status, status + 1, di.num_sms, stream));
   return KD_OK;
 }
 

@@ -78,17 +78,28 @@ cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, con
                               int nsplit, int T, int K, int32_t* out_id, float* out_val,
                               cudaStream_t stream);
 
-// kernels_rkl.cu — reverse KL over the cached ids (CUDA cores, one warp per token)
-int rkl_blocks(int T);
-cudaError_t launch_rkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* idx,
-                               const float* logit, const uint8_t* mask, int T, int d, int K, int V,
-                               float inv_tau, float* token_rkl, double* block_sums, int* n_count,
-                               int* status, cudaStream_t stream);
-// Counts the unmasked tokens into *n_count (zeroed by the caller), then the gradient.
-cudaError_t launch_rkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* idx,
-                                const float* logit, const uint8_t* mask, int T, int d, int K, int V,
-                                float inv_tau, float grad_loss, int* n_count, uint16_t* dH,
-                                float* dW, int* status, int num_sms, cudaStream_t stream);
+// kernels_rkl.cu — reverse KL over the cached ids (CUDA cores; see the file)
+struct RklLayout {
+  long long n;        // T * K (id, position) pairs
+  long long n_tiles;  // radix-sort tiles
+  long long n_seg;    // dW segments
+  int passes, bits, nbins;
+  size_t off_bsum, fwd_total;  // the forward uses [0, fwd_total)
+  size_t off_G, off_keys[2], off_vals[2], off_hist, off_scan, off_bstart, off_bend, off_part;
+  size_t total;
+};
+RklLayout rkl_layout(long long T, long long d, int K, long long V, size_t header);
+// count -> per-token RKL (+ grad_z) -> loss. *n_count must start at 0.
+cudaError_t rkl_forward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
+                        const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
+                        int K, int V, float inv_tau, float* token_rkl, float* grad_z, float* loss,
+                        void* ws, int* status, int* n_count, int num_sms, cudaStream_t stream);
+// [recompute G] -> dH -> sort by id -> dW segments -> dW fix-up. *n_count must start at 0.
+cudaError_t rkl_backward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
+                         const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
+                         int K, int V, float inv_tau, const float* grad_z, float grad_loss,
+                         uint16_t* dH, float* dW, int accumulate, void* ws, int* status,
+                         int* n_count, int num_sms, cudaStream_t stream);
 
 // kernels_gemm.cu — tcgen05 GEMMs (see tc_gemm.cuh for the epilogues)
 enum GemmKind {

@@ -74,8 +74,8 @@ _SIGS = {
                                              _P, _P, _P, _P]),
     "kd_rkl_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_kl_problem)]),
     "kd_rkl_forward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P, _P,
-                                      _P, ctypes.c_size_t, _P]),
-    "kd_rkl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P,
+                                      _P, _P, ctypes.c_size_t, _P]),
+    "kd_rkl_backward": (ctypes.c_int, [ctypes.POINTER(kd_kl_problem), _P, _P, _P, _P, _P, _P,
                                        ctypes.c_float, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
                                        _P]),
     "kd_lmhead_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kd_topk_problem)]),
@@ -335,25 +335,36 @@ def _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace):
 
 
 def kd_rkl_forward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0,
-                   want_token_rkl=False, loss=None, token_rkl=None, workspace=None, stream=None):
-    """Reverse KL over the cached ids. Returns (loss [1] fp32, token_rkl [T] fp32 or None)."""
+                   want_token_rkl=False, want_grad_z=False, loss=None, token_rkl=None, grad_z=None,
+                   workspace=None, stream=None):
+    """Reverse KL over the cached ids. Returns (loss [1] fp32, token_rkl [T] fp32 or None,
+    grad_z [T,K] fp32 or None)."""
     p, workspace = _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace)
     dev = H.device
     loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
     if want_token_rkl and token_rkl is None:
         token_rkl = torch.empty(H.shape[0], dtype=torch.float32, device=dev)
+    if want_grad_z and grad_z is None:
+        grad_z = torch.empty(tuple(topk_idx.shape), dtype=torch.float32, device=dev)
+    if grad_z is not None:
+        _check(grad_z, "grad_z", torch.float32, tuple(topk_idx.shape))
     rc = load().kd_rkl_forward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
                                _ptr(topk_logit), _ptr(mask), _ptr(loss), _ptr(token_rkl),
-                               _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+                               _ptr(grad_z), _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
     if rc != KD_OK:
         raise KDKLError(rc, "kd_rkl_forward")
-    return loss, token_rkl
+    return loss, token_rkl, grad_z
 
 
-def kd_rkl_backward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0, grad_loss=1.0,
-                    dH=None, dW=None, accumulate_dW=False, workspace=None, stream=None):
-    """Backward of grad_loss * reverse-KL loss. Returns (dH [T,d] bf16, dW [V,d] fp32)."""
+def kd_rkl_backward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0, grad_z=None,
+                    grad_loss=1.0, dH=None, dW=None, accumulate_dW=False, workspace=None,
+                    stream=None):
+    """Backward of grad_loss * reverse-KL loss. Returns (dH [T,d] bf16, dW [V,d] fp32).
+    grad_z from kd_rkl_forward (same inputs) skips the logit recompute."""
     p, workspace = _rkl_args(H, W, topk_idx, topk_logit, mask, temperature, workspace)
+    if grad_z is not None:
+        _check(grad_z, "grad_z", torch.float32, tuple(topk_idx.shape))
     dev = H.device
     T, d = H.shape
     dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dH is None else dH
@@ -362,9 +373,9 @@ def kd_rkl_backward(H, W, topk_idx, topk_logit, mask=None, *, temperature=1.0, g
             raise ValueError("accumulate_dW needs an existing dW")
         dW = torch.empty((W.shape[0], d), dtype=torch.float32, device=dev)
     rc = load().kd_rkl_backward(ctypes.byref(p), _ptr(H), _ptr(W), _ptr(topk_idx),
-                                _ptr(topk_logit), _ptr(mask), float(grad_loss), _ptr(dH), _ptr(dW),
-                                1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(),
-                                _stream_ptr(stream))
+                                _ptr(topk_logit), _ptr(mask), _ptr(grad_z), float(grad_loss),
+                                _ptr(dH), _ptr(dW), 1 if accumulate_dW else 0, _ptr(workspace),
+                                workspace.numel(), _stream_ptr(stream))
     if rc != KD_OK:
         raise KDKLError(rc, "kd_rkl_backward")
     return dH, dW

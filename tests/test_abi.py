@@ -122,13 +122,13 @@ def test_workspace_linear_in_T_no_TxV(lib, name):
 def _rkl_fwd(lib, p, H=16, ws=256, loss=64):
     P = ctypes.c_void_p
     return lib.kd_rkl_forward(ctypes.byref(p), P(H), P(16), P(16), P(16), None, P(loss), None,
-                              P(ws), 1 << 30, None)
+                              None, P(ws), 1 << 30, None)
 
 
 def _rkl_bwd(lib, p, dH=4096, dW=8192, g=1.0):
     P = ctypes.c_void_p
-    return lib.kd_rkl_backward(ctypes.byref(p), P(16), P(16), P(16), P(16), None, g, P(dH), P(dW),
-                               0, P(256), 1 << 30, None)
+    return lib.kd_rkl_backward(ctypes.byref(p), P(16), P(16), P(16), P(16), None, None, g, P(dH),
+                               P(dW), 0, P(256), 1 << 30, None)
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -152,6 +152,13 @@ def test_rkl_pointer_errors_and_workspace(lib):
     assert _rkl_bwd(lib, p, dW=0) == 1
     assert _rkl_bwd(lib, p, dH=24) == 3
     assert _rkl_bwd(lib, p, g=float("inf")) == 1
-    # header plus 8 bytes per 8 tokens: linear in T, independent of V and d
-    sizes = [kdkl.kd_rkl_workspace_size(T, 2880, 201088, 100) for T in (8192, 16384, 32768)]
-    assert sizes[0] < sizes[1] < sizes[2] <= 256 + 32768 + 256
+    # linear in T (no T x V term): per pair the gradient, two sort buffers and
+    # the dW partials (2 rows of d fp32 per 256 pairs); 8 bytes per vocabulary row
+    T, d, V, K = 32768, 2880, 201088, 100
+    sizes = [kdkl.kd_rkl_workspace_size(t, d, V, K) for t in (T // 4, T // 2, T)]
+    assert sizes[0] < sizes[1] < sizes[2]
+    per_pair = 4 * 5 + 2 * d * 4 / 256 + 1  # + radix histograms (<= 1 byte per pair)
+    assert sizes[2] <= T * K * per_pair + 8 * (V + 1) + T + (1 << 20)
+    assert abs((sizes[2] - sizes[1]) - (sizes[1] - sizes[0]) * 2) < (1 << 20)
+    # T * K must stay below 2^31
+    assert kdkl.kd_rkl_workspace_size(1 << 24, 64, 1000, 200) == 0

@@ -23,32 +23,35 @@ def kdkl():
     return m
 
 
-def _run(kdkl, x, tau, grad_loss=0.8, dW_init=None):
+def _run(kdkl, x, tau, grad_loss=0.8, dW_init=None, use_grad_z=True):
     g = {k: v.cuda() for k, v in x.items()}
-    loss, tok = kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
-                                    temperature=tau, want_token_rkl=True)
+    loss, tok, gz = kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
+                                        temperature=tau, want_token_rkl=True, want_grad_z=True)
     dW = None if dW_init is None else dW_init.cuda().clone()
     dH, dW = kdkl.kd_rkl_backward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
-                                  temperature=tau, grad_loss=grad_loss, dW=dW,
-                                  accumulate_dW=dW_init is not None)
+                                  temperature=tau, grad_z=gz if use_grad_z else None,
+                                  grad_loss=grad_loss, dW=dW, accumulate_dW=dW_init is not None)
     torch.cuda.synchronize()
     return (loss.item(), tok.cpu().numpy().astype(np.float64),
-            dH.float().cpu().numpy().astype(np.float64), dW.cpu().numpy().astype(np.float64))
+            dH.float().cpu().numpy().astype(np.float64), dW.cpu().numpy().astype(np.float64),
+            gz.cpu().numpy().astype(np.float64))
 
 
 def _check(x, tau, got, grad_loss=0.8, dW_base=None):
-    loss, tok, dH, dW = got
+    loss, tok, dH, dW, gz = got
     H, W, idx, logit, mask = to_oracle(x)
     r_loss, r_tok, _ = ok.reverse_kl_forward(H, W, idx, logit, mask, tau)
+    r_gz = ok.reverse_kl_grad_z(H, W, idx, logit, mask, tau)
     r_dH, r_dW = ok.reverse_kl_backward(H, W, idx, logit, mask, tau, grad_loss)
     if dW_base is not None:
         r_dW = r_dW + dW_base
     assert abs(loss - r_loss) <= LOSS_RTOL * abs(r_loss) + 1e-6, (loss, r_loss)
     assert np.abs(tok - r_tok).max() <= 1e-3 * max(1.0, np.abs(r_tok).max())
+    assert rel_l2(gz, r_gz) <= GRAD_REL_L2
     assert rel_l2(dH, r_dH) <= GRAD_REL_L2
     assert rel_l2(dW, r_dW) <= GRAD_REL_L2
     # masked tokens: no gradient at all
-    assert np.all(dH[mask == 0] == 0.0)
+    assert np.all(dH[mask == 0] == 0.0) and np.all(gz[mask == 0] == 0.0)
 
 
 @pytest.mark.parametrize("tau", [1.0, 2.0, 0.6])
@@ -65,10 +68,14 @@ def test_against_oracle(kdkl, tau, shape):
     x = make_inputs(w, seed=21)
     got = _run(kdkl, x, tau)
     if K == 1:
-        loss, tok, dH, dW = got
+        loss, tok, dH, dW, gz = got
         assert loss == 0.0 and np.all(tok == 0.0) and np.all(dH == 0.0) and np.all(dW == 0.0)
+        assert np.all(gz == 0.0)
         return
     _check(x, tau, got)
+    # the backward's own recompute of grad_z gives the same gradients
+    again = _run(kdkl, x, tau, use_grad_z=False)
+    assert np.array_equal(again[2], got[2]) and np.array_equal(again[3], got[3])
 
 
 def test_neg_inf_entries_and_repeated_ids(kdkl):
@@ -100,7 +107,7 @@ def test_matching_distributions_give_zero(kdkl):
     x = make_inputs(w, seed=24)
     H, W, idx = x["H"].float(), x["W"].float(), x["topk_idx"].long()
     x["topk_logit"] = (torch.gather(H @ W.T, 1, idx) + 2.5).contiguous()
-    loss, tok, dH, dW = _run(kdkl, x, 1.0)
+    loss, tok, dH, dW, _ = _run(kdkl, x, 1.0)
     assert abs(loss) < 1e-5 and np.abs(tok).max() < 1e-5
     assert np.abs(dH).max() < 1e-4 and np.abs(dW).max() < 1e-4
 
@@ -109,17 +116,36 @@ def test_all_masked_and_empty(kdkl):
     w = WORKLOADS["small"].with_(T=40, d=32, V=100, K=4)
     x = make_inputs(w, seed=25)
     x["mask"][:] = 0
-    loss, tok, dH, dW = _run(kdkl, x, 1.0)
+    loss, tok, dH, dW, gz = _run(kdkl, x, 1.0)
     assert loss == 0.0 and np.all(dH == 0.0) and np.all(dW == 0.0)
     assert np.all(np.isfinite(tok)) and tok.max() > 0.0  # per-token values before masking
+    assert np.all(gz == 0.0)
     H = torch.zeros((0, 32), dtype=torch.bfloat16, device="cuda")
     W = x["W"].cuda()
     idx = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
     lg = torch.zeros((0, 4), dtype=torch.float32, device="cuda")
-    loss, _ = kdkl.kd_rkl_forward(H, W, idx, lg)
+    loss, _, _ = kdkl.kd_rkl_forward(H, W, idx, lg)
     dH, dW = kdkl.kd_rkl_backward(H, W, idx, lg)
     torch.cuda.synchronize()
     assert loss.item() == 0.0 and dH.shape == (0, 32) and torch.count_nonzero(dW).item() == 0
+
+
+def test_backward_is_bitwise_reproducible_and_heavy_ids(kdkl):
+    """A few ids named by every token (buckets far longer than one dW segment)
+    next to rare ones; two backward calls give identical bits."""
+    w = WORKLOADS["small"].with_(T=1500, d=200, V=5000, K=24, tau=1.0, seq_len=500,
+                                 pad_frac=0.1)
+    x = make_inputs(w, seed=28)
+    idx = x["topk_idx"].numpy()
+    heavy = np.array([7, 4000, 4001], dtype=np.int32)
+    for j, h in enumerate(heavy):  # keep rows duplicate-free: replace where absent
+        col = idx[:, j]
+        absent = ~(idx == h).any(axis=1)
+        col[absent] = h
+    got = _run(kdkl, x, 1.0)
+    _check(x, 1.0, got)
+    again = _run(kdkl, x, 1.0)
+    assert np.array_equal(got[2], again[2]) and np.array_equal(got[3], again[3])
 
 
 def test_index_out_of_range_is_reported(kdkl):
@@ -155,10 +181,11 @@ def test_full_size_sparse_mask(kdkl, name):
     mask[torch.from_numpy(S)] = 1
     g = {k: v.cuda() for k, v in x.items()}
     g["mask"] = mask.cuda()
-    loss, tok = kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
-                                    temperature=w.tau, want_token_rkl=True)
+    loss, tok, gz = kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"],
+                                        g["mask"], temperature=w.tau, want_token_rkl=True,
+                                        want_grad_z=True)
     dH, dW = kdkl.kd_rkl_backward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"],
-                                  temperature=w.tau, grad_loss=1.0)
+                                  temperature=w.tau, grad_z=gz, grad_loss=1.0)
     torch.cuda.synchronize()
     idx_S = x["topk_idx"].numpy()[S].astype(np.int64)
     touched, local = np.unique(idx_S, return_inverse=True)

@@ -56,16 +56,17 @@ def csrc_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def recorded_traffic(kernel: str, workload: str = WORKLOAD):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    summary was taken on the current kernel sources; otherwise None."""
+    summary was taken on the current kernel sources and this workload;
+    otherwise None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("csrc_sha256_16") != csrc_digest() or d.get("workload") != WORKLOAD:
+    if d.get("csrc_sha256_16") != csrc_digest() or d.get("workload") != workload:
         return None
     k = d.get("kernels", {}).get(kernel)
     return None if k is None else float(k["dram_bytes_per_launch"])
@@ -276,6 +277,7 @@ def run_kdkl(args):
         # per step for each of the four GEMM kinds, split over its launches
         rows = {n: (c, ms) for n, c, ms in per_kernel}
         dom = max(rows, key=lambda n: rows[n][1])
+        run_name = w.name if not args.tokens else ""  # traffic was recorded at full size
         dom_launches, dom_ms = rows[dom]
         if dom in GEMM_KERNELS:
             per_launch_flops = 2.0 * T * V * d * args.steps / dom_launches
@@ -286,10 +288,10 @@ def run_kdkl(args):
                     "peak_source": "%s bf16_tflops_sustained" % pk_src,
                     "flops_per_launch": per_launch_flops,
                     "avg_launch_ms": round(dom_ms / dom_launches, 4),
-                    "traffic": recorded_traffic(dom)}
+                    "traffic": recorded_traffic(dom, run_name)}
         else:
             roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": None, "traffic": recorded_traffic(dom)}
+                    "unit": "GB/s", "frac": None, "traffic": recorded_traffic(dom, run_name)}
         # CPU baseline: the fp64 oracle on a bounded token sample, this host
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -402,7 +404,7 @@ def run_topk(args):
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
                      "peak_source": "%s bf16_tflops_sustained" % pk_src,
-                     "traffic": recorded_traffic("topk_gemm")},
+                     "traffic": recorded_traffic("topk_gemm", w.name if not args.tokens else "")},
         "gpu_launches": kdkl.kd_launch_count() - launches0,
         "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
         "clocks": clocks.summary(),
@@ -498,7 +500,7 @@ def run_rkl(args):
                      "peak_source": "%s hbm_gbs" % pk_src, "bytes_per_launch": algo,
                      "pair_gather_gbs": round(gather_gbs, 1),
                      "pair_gather_frac": round(gather_gbs / pk["hbm_gbs"], 4),
-                     "traffic": None},
+                     "traffic": recorded_traffic(dom, w.name if not args.tokens else "")},
         "gpu_launches": kdkl.kd_launch_count() - launches0,
         "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
         "clocks": clocks.summary(),

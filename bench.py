@@ -150,13 +150,16 @@ def barrier(world: int):
 
 # --------------------------------------------------------------- oracle timing
 
-def oracle_sample_step(x_np, w, rows):
-    """fp64 oracle forward + backward on a sample of token rows (all V, all d)."""
+def oracle_sample_step(x_np, w, rows, block: int = 1024):
+    """fp64 oracle forward + backward on a sample of token rows (all V, all d),
+    1024 rows at a time so the dense logit block stays a few GB."""
     import oracle.kl_oracle as ok
     H, W, idx, logit, mask = x_np
-    Hs, idxs, lgs, ms = H[rows], idx[rows], logit[rows], mask[rows]
-    ok.forward(Hs, W, idxs, lgs, ms, w.tau)
-    ok.backward(Hs, W, idxs, lgs, ms, w.tau, 1.0)
+    for b in range(0, len(rows), block):
+        r = rows[b:b + block]
+        Hs, idxs, lgs, ms = H[r], idx[r], logit[r], mask[r]
+        ok.forward(Hs, W, idxs, lgs, ms, w.tau)
+        ok.backward(Hs, W, idxs, lgs, ms, w.tau, 1.0)
 
 
 def oracle_arrays(x):
@@ -171,7 +174,7 @@ def time_oracle(x_np, w, n_tokens: int, repeats: int = 1):
     rng = np.random.default_rng(0)
     times = []
     for _ in range(repeats):
-        rows = np.sort(rng.choice(w.T, size=n_tokens, replace=False))
+        rows = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
         t0 = time.perf_counter()
         oracle_sample_step(x_np, w, rows)
         times.append(time.perf_counter() - t0)
@@ -179,6 +182,24 @@ def time_oracle(x_np, w, n_tokens: int, repeats: int = 1):
 
 
 # ------------------------------------------------------------------- main arm
+
+def apply_overrides(w, args):
+    """The workload with --tokens/--K/--tau/--chunk applied, and the name it is
+    reported under (the plain name when nothing is overridden)."""
+    kw = {}
+    if args.tokens:
+        kw["T"] = args.tokens
+    if args.K:
+        kw["K"] = args.K
+    if args.tau:
+        kw["tau"] = args.tau
+    if args.chunk:
+        kw["chunk"] = args.chunk
+    if not kw:
+        return w, w.name
+    w2 = w.with_(**kw)
+    return w2, "%s_T%d_K%d_tau%g_chunk%d" % (w.name, w2.T, w2.K, w2.tau, w2.chunk)
+
 
 def run_kdkl(args):
     from lm_head_top_gb300 import kdkl
@@ -192,9 +213,7 @@ def run_kdkl(args):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     kdkl.load()
-    w = WORKLOADS[args.workload]
-    if args.tokens:
-        w = w.with_(T=args.tokens)
+    w, wname = apply_overrides(WORKLOADS[args.workload], args)
     x = make_inputs(w, seed=rank, topk_device=dev)
     T, d, V, K = w.T, w.d, w.V, w.K
 
@@ -277,7 +296,7 @@ def run_kdkl(args):
         # per step for each of the four GEMM kinds, split over its launches
         rows = {n: (c, ms) for n, c, ms in per_kernel}
         dom = max(rows, key=lambda n: rows[n][1])
-        run_name = w.name if not args.tokens else ""  # traffic was recorded at full size
+        run_name = wname  # traffic is recorded for the plain workloads only
         dom_launches, dom_ms = rows[dom]
         if dom in GEMM_KERNELS:
             per_launch_flops = 2.0 * T * V * d * args.steps / dom_launches
@@ -301,7 +320,8 @@ def run_kdkl(args):
             cpu = {"value": round(n_cpu / t, 3), "unit": "tokens/s", "cores": os.cpu_count(),
                    "kind": "oracle",
                    "sample": "fp64 oracle forward+backward on %d random tokens of %s (all V=%d, "
-                             "d=%d; dense logits row block), %.1f s" % (n_cpu, WORKLOAD, V, d, t)}
+                             "d=%d; dense logits row blocks), %.1f s" % (min(n_cpu, T), wname, V,
+                                                                        d, t)}
         result = {
             "metric": METRIC,
             "value": round(tokens / (elapsed_ms / 1e3), 1),
@@ -314,9 +334,10 @@ def run_kdkl(args):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
-            "data": "synthetic (seeded; bf16 H~N(0,1), W~N(0,1/d); teacher top-100 half from "
-                    "the student's own top-100)",
-            "config": {"workload": w.name if not args.tokens else "%s_T%d" % (w.name, T), "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
+            "data": "synthetic (seeded; bf16 H~N(0,1), W~N(0,1/d); teacher top-%d %s)" % (
+                K, "half from the student's own top-%d" % K if w.teacher == "half_overlap"
+                else "uniform distinct ids"),
+            "config": {"workload": wname, "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
                        "tau": w.tau, "global_batch_tokens": T * world,
                        "parallelism": "dp%d (independent batches)" % world,
                        "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
@@ -423,9 +444,7 @@ def run_rkl(args):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     kdkl.load()
-    w = WORKLOADS[args.workload]
-    if args.tokens:
-        w = w.with_(T=args.tokens)
+    w, wname = apply_overrides(WORKLOADS[args.workload], args)
     x = make_inputs(w, seed=rank, topk_device=dev)
     T, d, V, K = w.T, w.d, w.V, w.K
     torch.cuda.reset_peak_memory_stats(dev)
@@ -491,7 +510,7 @@ def run_rkl(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s_rkl" % w.name if not args.tokens else "%s_T%d_rkl" % (w.name, T),
+        "config": {"workload": "%s_rkl" % wname,
                    "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "distinct_ids": distinct,
                    "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
         "peak_hbm_gib": round(torch.cuda.max_memory_allocated(dev) / 2 ** 30, 3),
@@ -500,7 +519,7 @@ def run_rkl(args):
                      "peak_source": "%s hbm_gbs" % pk_src, "bytes_per_launch": algo,
                      "pair_gather_gbs": round(gather_gbs, 1),
                      "pair_gather_frac": round(gather_gbs / pk["hbm_gbs"], 4),
-                     "traffic": recorded_traffic(dom, w.name if not args.tokens else "")},
+                     "traffic": recorded_traffic(dom, wname)},
         "gpu_launches": kdkl.kd_launch_count() - launches0,
         "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
         "clocks": clocks.summary(),
@@ -554,6 +573,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another workload's shapes, for profiling small cases")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
+    ap.add_argument("--K", type=int, default=0, help="override K (config sweeps)")
+    ap.add_argument("--tau", type=float, default=0.0, help="override the temperature")
+    ap.add_argument("--chunk", type=int, default=0, help="override chunk")
     args = ap.parse_args()
     if args.impl == "kdkl":
         args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps

@@ -230,12 +230,13 @@ def run_kdkl(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(gg):
+        s = torch.cuda.current_stream(dev)  # the capture stream inside a graph capture
         kdkl.kd_kl_forward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"],
                            temperature=w.tau, chunk=w.chunk, loss=loss, lse=lse, workspace=ws_f,
-                           stream=stream)
+                           stream=s)
         kdkl.kd_kl_backward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"], lse,
                             temperature=w.tau, chunk=w.chunk, grad_loss=1.0, dH=dH, dW=dW,
-                            workspace=ws_b, stream=stream)
+                            workspace=ws_b, stream=s)
 
     for _ in range(args.warmup):
         step(g)
@@ -264,6 +265,38 @@ def run_kdkl(args):
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     clk = clocks.summary()
     peak_hbm = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+
+    # ---- the same step captured once in a CUDA graph and replayed (launch-bound
+    # small shapes); reported beside the eager numbers
+    graph_res = None
+    if args.graph:
+        per_step = launches // args.steps
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(dev)
+        n0 = kdkl.kd_launch_count()
+        with torch.cuda.graph(graph):
+            step(g)
+        if kdkl.kd_launch_count() - n0 != per_step:
+            raise SystemExit("graph capture recorded %d launches, expected %d"
+                             % (kdkl.kd_launch_count() - n0, per_step))
+        for _ in range(args.warmup):
+            graph.replay()
+        gs = torch.cuda.current_stream(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        g0.record(gs)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(gs)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        gms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+        graph_res = {"value": round(T * world * args.steps / (gms / 1e3), 1), "unit": "tokens/s",
+                     "ms_per_step": round(gms / args.steps, 4),
+                     "gpu_launches": per_step * args.steps,
+                     "note": "one captured step replayed; eager numbers above"}
+        del graph
 
     # ---- end to end: pinned host inputs copied in, loss read back, every step
     e2e_ms, h2d = None, 0
@@ -354,6 +387,8 @@ def run_kdkl(args):
             "kernel_ms_per_step": {n: round(ms / args.steps, 3) for n, c, ms in per_kernel},
             "clocks": clk,
         }
+        if graph_res is not None:
+            result["graph"] = graph_res
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -576,6 +611,8 @@ def main():
     ap.add_argument("--K", type=int, default=0, help="override K (config sweeps)")
     ap.add_argument("--tau", type=float, default=0.0, help="override the temperature")
     ap.add_argument("--chunk", type=int, default=0, help="override chunk")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed")
     args = ap.parse_args()
     if args.impl == "kdkl":
         args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps

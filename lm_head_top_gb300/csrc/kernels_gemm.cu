@@ -1,6 +1,8 @@
 // Instantiations and launchers of the tcgen05 GEMM kernel for the four
 // contractions of the fused KL loss (forward logsumexp, backward recompute,
 // dH = G W, dW = G^T H).
+#include <atomic>
+
 #include "kdkl_internal.h"
 #include "tc_gemm.cuh"
 
@@ -16,15 +18,17 @@ cudaError_t launch_one(const char* name, const CUtensorMap& tmA, const CUtensorM
                        cudaStream_t stream) {
   auto kern = tc_gemm_kernel<EPI, A_MN, B_MN, BN, PAIR>;
   constexpr int smem = TileCfg<BN, PAIR>::SMEM_BYTES;
-  static bool attr_done[kMaxDevices] = {};
+  // Per device and instantiation; concurrent first calls may both set the
+  // attribute, which is harmless (same value).
+  static std::atomic<bool> attr_done[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   if (PAIR)
     return launch_kernel_cluster(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)smem, stream,
@@ -45,10 +49,11 @@ cudaError_t launch_pick(bool pair, const char* name, const CUtensorMap& tmA, con
 }  // namespace
 
 int pair_max_active_clusters() {
-  static int cached[kMaxDevices] = {};
+  static std::atomic<int> cached[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (cached[dev] > 0) return cached[dev];
+  const int known = cached[dev].load(std::memory_order_acquire);
+  if (known > 0) return known;
   // Every pair instantiation has the same block size and shared memory, so one
   // of them stands for all.
   auto kern = tc_gemm_kernel<EPI_LSE, false, false, LOGIT_BN, true>;
@@ -69,7 +74,7 @@ int pair_max_active_clusters() {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
-  cached[dev] = n;
+  cached[dev].store(n, std::memory_order_release);
   return n;
 }
 

@@ -32,6 +32,8 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "kdkl_internal.h"
 #include "tc_primitives.cuh"
@@ -684,7 +686,11 @@ static cudaError_t launch_forward_kernel(const char* name, const uint16_t* H, co
                                          float* G, double* bsum, int* status,
                                          cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
-  static size_t attr_bytes[2][kMaxDevices] = {};
+  // Largest dynamic shared memory set so far, per instantiation and device.
+  // The attribute is raised under a lock so that a smaller concurrent request
+  // cannot land after a larger one.
+  static std::atomic<size_t> attr_bytes[2][kMaxDevices] = {};
+  static std::mutex attr_mu;
   const bool stage = d <= RKL_STAGE_H_MAX_D;
   const size_t smem = RKL_WARPS * rkl_forward_smem_per_warp(d, K, stage);
   void (*kern)(const uint16_t*, const uint16_t*, const int32_t*, const float*, const uint8_t*, int,
@@ -694,10 +700,14 @@ static cudaError_t launch_forward_kernel(const char* name, const uint16_t* H, co
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (smem > attr_bytes[stage][dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_bytes[stage][dev] = smem;
+  std::atomic<size_t>& set = attr_bytes[stage][dev];
+  if (smem > set.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lk(attr_mu);
+    if (smem > set.load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      set.store(smem, std::memory_order_release);
+    }
   }
   return launch_kernel(name, kern, dim3(blocks_for(T, RKL_WARPS)), dim3(RKL_WARPS * 32), smem,
                        stream, H, W, idx, logit, mask, T, d, K, V, inv_tau, n_count, token_rkl, G,

@@ -314,6 +314,10 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   }
   f.nsplit = sp.nsplit;
   f.group_n = sp.group_n;
+  if (const char* g = getenv("KDKL_TOPK_GROUP")) {  // tuning: splits in flight per m-tile
+    const int gn = atoi(g);
+    if (gn > 0) f.group_n = std::min(gn, f.nsplit);
+  }
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
   f.cap = std::max(p.K + 64, std::min(512, p.K + topk_slack()));
   const size_t cand = (size_t)num_sms * BM * f.cap;  // one list per (CTA, row), any grid <= SMs

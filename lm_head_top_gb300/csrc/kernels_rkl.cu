@@ -41,7 +41,6 @@
 namespace kdkl {
 
 constexpr int RKL_WARPS = 8;
-constexpr int RKL_MAX_K = 512;  // entries per warp kept in shared memory
 constexpr int RADIX_TILE = 4096;
 constexpr int RADIX_THREADS = 256;
 constexpr int RADIX_ROUNDS = RADIX_TILE / RADIX_THREADS;

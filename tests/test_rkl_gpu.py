@@ -165,7 +165,7 @@ def test_index_out_of_range_is_reported(kdkl):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["gptoss20b_32k", "llama3b_8k"])
+@pytest.mark.parametrize("name", ["gptoss20b_32k", "llama3b_8k", "padded_4x8k", "toyproj_256k"])
 def test_full_size_sparse_mask(kdkl, name):
     """Full-size shapes. Only a sampled token set S counts (m = 0 elsewhere),
     so the oracle needs only the rows of S and the rows of W at their ids: it

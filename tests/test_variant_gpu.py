@@ -81,3 +81,45 @@ def test_label_out_of_range_is_reported(kdkl):
     kdkl.kd_kl_forward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], y,
                           chunk=16, alpha=0.5, workspace=ws)
     assert kdkl.kd_kl_check_status(ws) == 4
+
+
+@pytest.mark.slow
+def test_full_size_sparse_mask(kdkl):
+    """The GPT-OSS-like head at 32,768 tokens in the benchmark's launch
+    configuration, with only a sampled token set S counted (m = 0 elsewhere).
+    The oracle then needs only the rows of S: exact loss, lse and lse1 on S,
+    dH on S, and every row of dW; rows outside S get no gradient."""
+    w = WORKLOADS["gptoss20b_32k"].with_(tau=2.0)
+    x = make_inputs(w, seed=41, topk_device="cuda")
+    T, V = w.T, w.V
+    rng = np.random.default_rng(9)
+    S = np.unique(np.concatenate([[0, 255, 256, T // 2, T - 1], rng.choice(T, 120, replace=False)]))
+    mask = np.zeros(T, dtype=np.uint8)
+    mask[S] = 1
+    y = rng.integers(0, V, T).astype(np.int32)
+    g = {k: v.cuda() for k, v in x.items()}
+    g["mask"] = torch.from_numpy(mask).cuda()
+    yl = torch.from_numpy(y).cuda()
+    loss, lse, lse1, _ = kdkl.kd_kl_forward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"],
+                                               g["mask"], yl, temperature=w.tau, chunk=w.chunk,
+                                               alpha=0.4, scale_tau_sq=True)
+    dH, dW = kdkl.kd_kl_backward_ex(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], yl,
+                                    lse, lse1, temperature=w.tau, chunk=w.chunk, alpha=0.4,
+                                    scale_tau_sq=True, grad_loss=1.0)
+    torch.cuda.synchronize()
+    s_dev = torch.from_numpy(S).cuda()
+    H_S = ok.bf16_bits_to_f64(x["H"][torch.from_numpy(S)].view(torch.int16).numpy())
+    Wn = ok.bf16_bits_to_f64(x["W"].view(torch.int16).numpy())
+    idx_S = x["topk_idx"].numpy()[S].astype(np.int64)
+    lg_S = x["topk_logit"].numpy()[S].astype(np.float64)
+    ones = np.ones(len(S), dtype=np.uint8)
+    r_loss, r_lse, r_lse1, _ = ok.forward_mixed(H_S, Wn, idx_S, lg_S, ones, w.tau, 0.4, True, y[S])
+    assert abs(loss.item() - r_loss) <= LOSS_RTOL * abs(r_loss)
+    assert np.abs(lse[s_dev].cpu().numpy() - r_lse).max() <= LSE_ATOL
+    assert np.abs(lse1[s_dev].cpu().numpy() - r_lse1).max() <= LSE_ATOL
+    r_dH, r_dW = ok.backward_mixed(H_S, Wn, idx_S, lg_S, ones, w.tau, 0.4, True, y[S], 1.0)
+    assert rel_l2(dH[s_dev].float().cpu().numpy(), r_dH) <= GRAD_REL_L2
+    assert rel_l2(dW.double().cpu().numpy(), r_dW) <= GRAD_REL_L2
+    keep = torch.zeros(T, dtype=torch.bool, device="cuda")
+    keep[s_dev] = True
+    assert torch.count_nonzero(dH[~keep]).item() == 0

@@ -313,7 +313,18 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
     sp.group_n = std::min(sp.group_n, max_ns);
   }
   f.nsplit = sp.nsplit;
+  // Fewer splits of a row in flight than the logit GEMMs use: a split that
+  // starts after another split of its rows has compacted begins from the
+  // threshold that split published, so it appends and compacts far less.
+  // Bounded by L2 room for the A rows of the m-tiles in flight (~half of L2).
+  // At the GPT-OSS-like head, 2 instead of 5 cut the kernel's cycles by 9 %.
   f.group_n = sp.group_n;
+  {
+    const double a_tile = (double)tile_m * (double)p.d * 2.0;
+    int g = 2;
+    while (g < sp.group_n && ceil_div(procs, g) * a_tile > 64.0 * 1024 * 1024) ++g;
+    f.group_n = std::min(sp.group_n, g);
+  }
   if (const char* g = getenv("KDKL_TOPK_GROUP")) {  // tuning: splits in flight per m-tile
     const int gn = atoi(g);
     if (gn > 0) f.group_n = std::min(gn, f.nsplit);

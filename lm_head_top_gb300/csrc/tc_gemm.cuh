@@ -512,6 +512,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       for (int n = nb; n < ne; ++n) {
+        if (EPI == EPI_TOPK) {
+          // While the next accumulator is not ready, compact rows whose lists
+          // are past half their slack: work moved out of the bursts in which
+          // many rows must compact before the next 32 appends (and the MMA
+          // waits on this warp). At most 32 rows per wait.
+          const int watermark = (ep.topk_cap + ep.K) / 2;
+          for (int spins = 0; spins < 32; ++spins) {
+            if (__any_sync(0xffffffffu, mbar_test_wait(tfull_bar(acc), acc_phase))) break;
+            const uint32_t want = __ballot_sync(0xffffffffu, cnt > watermark);
+            if (!want) break;
+            const int i = __ffs(want) - 1;
+            const int ni = __shfl_sync(0xffffffffu, cnt, i);
+            const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
+            const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
+            if (lane == i) {
+              th = fmaxf(th, thi);
+              cnt = ep.K;
+              atomicMax(rkey, f32_order_key(thi));
+            }
+          }
+        }
         bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status, limit);
         got = __all_sync(0xffffffffu, got);
         if (!got) {

@@ -331,7 +331,8 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   }
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
   f.cap = std::max(p.K + 64, std::min(512, p.K + topk_slack()));
-  const size_t cand = (size_t)num_sms * BM * f.cap;  // one list per (CTA, row), any grid <= SMs
+  // two list banks per (CTA, row), any grid <= SMs
+  const size_t cand = (size_t)num_sms * BM * 2 * f.cap;
   const size_t unit = (size_t)f.nsplit * p.T * p.K;
   size_t o = kHeaderBytes;
   f.off_cand = o; o = align256(o + cand * 8);

@@ -461,6 +461,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     const uint32_t tempty_remote0 = PAIR ? mapa_shared(tempty_bar(0), 0) : 0u;
+    // EPI_TOPK: each (CTA, row) has two list banks. When a unit ends, the warp
+    // switches bank and finishes the old unit's rows later (compaction to K
+    // and write-out, one row at a time), in the waits for the next unit's
+    // accumulators, instead of in one burst at the unit boundary.
+    int bank = 0;
+    uint32_t pend = 0u;  // rows of the finished unit still to write (warp-uniform)
+    int pend_cnt = 0;    // this lane's list length in that unit
+    int pend_bank = 0, pend_s = 0, pend_r0 = 0;
+    auto list_of = [&](int row_in_warp, int b) {
+      return ep.cand + (((long long)blockIdx.x * BM + q * 32 + row_in_warp) * 2 + b) * ep.topk_cap;
+    };
+    auto finalize_row = [&](int i) {  // warp-collective
+      const int ni = __shfl_sync(0xffffffffu, pend_cnt, i);
+      float2* li = list_of(i, pend_bank);
+      if (ni > ep.K) {
+        const float thi = topk_compact_row(li, ni, ep.K);
+        if (lane == 0) atomicMax(ep.row_key + ep.row0 + pend_r0 + i, f32_order_key(thi));
+      }
+      __syncwarp();
+      const int nk = min(ni, ep.K);
+      const long long o = ((long long)pend_s * ep.T + ep.row0 + pend_r0 + i) * ep.K;
+      for (int k = lane; k < ep.K; k += 32) {
+        const float2 c = k < nk ? li[k] : make_float2(-INFINITY, __int_as_float(-1));
+        ep.unit_val[o + k] = c.x;
+        ep.unit_id[o + k] = __float_as_int(c.y);
+      }
+    };
     for (int u = group0; ok && u < sh.units; u += groups) {
       int m, s, nb, ne;
       unit_coords(sh, u, m, s, nb, ne);
@@ -479,7 +506,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t* rkey = nullptr;
       if (EPI == EPI_TOPK) {
         row_ok = r < ep.rows;
-        c_list = ep.cand + ((long long)blockIdx.x * BM + r_in_tile) * ep.topk_cap;
+        c_list = list_of(lane, bank);
         if (row_ok) {
           rkey = ep.row_key + ep.row0 + r;
           th = topk_shared_threshold(rkey);
@@ -520,12 +547,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int watermark = (ep.topk_cap + ep.K) / 2;
           for (int spins = 0; spins < 32; ++spins) {
             if (__any_sync(0xffffffffu, mbar_test_wait(tfull_bar(acc), acc_phase))) break;
+            if (pend) {  // the finished unit's rows come first
+              const int i = __ffs(pend) - 1;
+              pend &= pend - 1u;
+              finalize_row(i);
+              continue;
+            }
             const uint32_t want = __ballot_sync(0xffffffffu, cnt > watermark);
             if (!want) break;
             const int i = __ffs(want) - 1;
             const int ni = __shfl_sync(0xffffffffu, cnt, i);
-            const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
-            const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
+            const float thi = topk_compact_row(list_of(i, bank), ni, ep.K);
             if (lane == i) {
               th = fmaxf(th, thi);
               cnt = ep.K;
@@ -556,8 +588,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const int i = __ffs(need) - 1;
               need &= need - 1u;
               const int ni = __shfl_sync(0xffffffffu, cnt, i);
-              const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
-              const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
+              const float thi = topk_compact_row(list_of(i, bank), ni, ep.K);
               if (lane == i) {
                 th = fmaxf(th, thi);
                 cnt = ep.K;
@@ -692,27 +723,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       if (!ok) break;
       if (EPI == EPI_TOPK) {
-        // final reduction to the split's top-K of every row, then write it out
-        uint32_t need = __ballot_sync(0xffffffffu, cnt > ep.K);
-        while (need) {
-          const int i = __ffs(need) - 1;
-          need &= need - 1u;
-          const int ni = __shfl_sync(0xffffffffu, cnt, i);
-          const long long slot_i = ((long long)blockIdx.x * BM + q * 32 + i) * ep.topk_cap;
-          const float thi = topk_compact_row(ep.cand + slot_i, ni, ep.K);
-          if (lane == i) {
-            cnt = ep.K;
-            atomicMax(rkey, f32_order_key(thi));
-          }
+        // Hand this unit's lists over to the deferred final step. Rows still
+        // pending from the unit before (only when units are a few tiles long)
+        // are finished first, since their bank is about to be reused.
+        while (pend) {
+          const int i = __ffs(pend) - 1;
+          pend &= pend - 1u;
+          finalize_row(i);
         }
-        if (row_ok) {
-          const long long o = ((long long)s * ep.T + ep.row0 + r) * ep.K;
-          for (int k = 0; k < ep.K; ++k) {
-            const float2 c = k < cnt ? c_list[k] : make_float2(-INFINITY, __int_as_float(-1));
-            ep.unit_val[o + k] = c.x;
-            ep.unit_id[o + k] = __float_as_int(c.y);
-          }
-        }
+        pend = __ballot_sync(0xffffffffu, row_ok);
+        pend_cnt = cnt;
+        pend_bank = bank;
+        pend_s = s;
+        pend_r0 = m * TILE_M + (int)rank * BM + q * 32;
+        bank ^= 1;
       }
       if (IS_LSE && row_ok) {
         const long long o = (long long)s * ep.T + ep.row0 + r;
@@ -723,6 +747,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           ep.ps1[o] = ep.same_tau ? run_sum : run_s1;
           ep.pzl[o] = zl;
         }
+      }
+    }
+    if (EPI == EPI_TOPK && ok) {
+      while (pend) {
+        const int i = __ffs(pend) - 1;
+        pend &= pend - 1u;
+        finalize_row(i);
       }
     }
   }

@@ -113,3 +113,18 @@ def test_cache_feeds_the_loss(kdkl):
     r_loss = ok.forward(H64, W64, idx.cpu().numpy(), val.cpu().numpy().astype(np.float64),
                         np.ones(200, np.uint8), 1.0)[0]
     assert abs(loss.item() - r_loss) <= 1e-3 * abs(r_loss)
+
+
+@pytest.mark.slow
+def test_gptoss_full_size_sampled_rows(kdkl):
+    """The benchmark's launch configuration: all 32,768 tokens of the
+    GPT-OSS-like head, K = 100 (10 vocabulary splits, two in flight per m-tile,
+    deferred unit finals). Sampled rows (tile and split edges, the last rows,
+    random ones) against the oracle."""
+    w = WORKLOADS["gptoss20b_32k"].with_(teacher="uniform")
+    ids, vals, H64, W64, _ = _run(kdkl, w, 100)
+    T = w.T
+    rows = np.unique(np.concatenate([[0, 255, 256, T // 2, T - 257, T - 256, T - 1],
+                                     np.random.default_rng(1).choice(T, 40, replace=False)]))
+    exact = check_rows(ids, vals, H64, W64, 100, rows)
+    assert exact >= 0.8 * len(rows)

@@ -527,7 +527,7 @@ def run_rkl(args):
     distinct = int(np.unique(x["topk_idx"].numpy()).size)
     pairs = T * K
     algo_bytes = {
-        "rkl_forward": distinct * d * 2 + T * d * 2 + pairs * 8 + T + pairs * 4,
+        "rkl_z_segment": distinct * d * 2 + T * d * 2 + pairs * 12,
         "rkl_dH": distinct * d * 2 + pairs * 8 + T * d * 2,
         "rkl_dW_segment": T * d * 2 + pairs * 12 + distinct * d * 4,
     }
@@ -536,8 +536,8 @@ def run_rkl(args):
     c, ms = rows[dom]
     algo = algo_bytes[dom]
     achieved = algo / (ms / c / 1e3) / 1e9
-    # what the design streams: one row (W for rkl_forward and rkl_dH, H for the
-    # dW segments) of d bf16 per (token, id) pair, whatever the cache hits
+    # what the design streams: one row (W for rkl_dH, H for the z and dW
+    # segments) of d bf16 per (token, id) pair, whatever the cache hits
     gather_gbs = pairs * d * 2 / (ms / c / 1e3) / 1e9
     return {
         "metric": "reverse KL over the cached ids fwd+bwd tokens/s", "path": "rkl",

@@ -84,17 +84,18 @@ struct RklLayout {
   long long n_tiles;  // radix-sort tiles
   long long n_seg;    // dW segments
   int passes, bits, nbins;
-  size_t off_bsum, fwd_total;  // the forward uses [0, fwd_total)
-  size_t off_G, off_keys[2], off_vals[2], off_hist, off_scan, off_bstart, off_bend, off_part;
+  size_t off_bsum;
+  size_t off_G, off_z, off_keys[2], off_vals[2], off_hist, off_scan, off_bstart, off_bend, off_part;
   size_t total;
 };
 RklLayout rkl_layout(long long T, long long d, int K, long long V, size_t header);
-// count -> per-token RKL (+ grad_z) -> loss. *n_count must start at 0.
+// count -> sort by id -> z per (token, id) pair -> per-token RKL (+ grad_z) -> loss.
+// *n_count must start at 0.
 cudaError_t rkl_forward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
                         const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
                         int K, int V, float inv_tau, float* token_rkl, float* grad_z, float* loss,
                         void* ws, int* status, int* n_count, int num_sms, cudaStream_t stream);
-// [recompute G] -> dH -> sort by id -> dW segments -> dW fix-up. *n_count must start at 0.
+// [recompute G, or sort by id] -> dH -> dW segments -> dW fix-up. *n_count must start at 0.
 cudaError_t rkl_backward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
                          const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
                          int K, int V, float inv_tau, const float* grad_z, float grad_loss,

@@ -9,10 +9,11 @@
 //
 // Kernels (all CUDA-core; the work is a sparse gather, not a contraction):
 //   rkl_count      unmasked-token count N
-//   rkl_forward    one warp per token: H_t staged in shared memory, the K
-//                  rows of W read four at a time against it, the restricted
-//                  softmaxes, RKL_t, optionally G[t,k] = dL/dz at the ids
-//                  (grad_loss = 1)
+//   rkl_z_segment  z for every (token, id) pair, vocabulary-major over the
+//                  pairs sorted by id: each named row of W read once per
+//                  segment, the tokens' rows of H streamed against it
+//   rkl_forward    one warp per token: the restricted softmaxes of its K z,
+//                  RKL_t, optionally G[t,k] = dL/dz at the ids (grad_loss = 1)
 //   rkl_dH         one warp per token: dH_t = g * sum_k G[t,k] W[idx_k]
 //   radix_hist / scan_* / radix_scatter / bucket_bounds
 //                  stable LSD radix sort of the T*K (id, t*K+k) pairs by id, so
@@ -32,8 +33,6 @@
 #include <stdint.h>
 
 #include <algorithm>
-#include <atomic>
-#include <mutex>
 
 #include "kdkl_internal.h"
 #include "tc_primitives.cuh"
@@ -106,50 +105,19 @@ __device__ __forceinline__ void load_slices(uint4 (&w)[RB][4], const uint16_t* _
   }
 }
 
-// z[k] = H_t . W[idx_k] for the warp's token into zs (shared). ZU ids at a
-// time: one sweep over d reads ZU rows of W together (lane-strided 16-byte
-// chunks) against H_t, which is staged in shared memory when hs != nullptr
-// (read from global memory otherwise), then one warp sum per id. Returns false
-// (and flags the status) if an id is out of range; that entry reads row 0 and
-// its z is discarded.
-constexpr int ZU = 4;
-
-__device__ bool rkl_gather_logits(const uint16_t* __restrict__ Ht, uint4* hs,
-                                  const uint16_t* __restrict__ W, const int32_t* __restrict__ irow,
-                                  int d, int K, int V, float* zs, int* status) {
+// z[k] for the warp's token from a buffer the segment kernel filled (one
+// float per (token, id) pair). Returns false (and flags the status) if an id is
+// out of range; such entries hold 0.
+__device__ bool rkl_load_logits(const int32_t* __restrict__ irow, const float* __restrict__ zrow,
+                                int K, int V, float* zs, int* status) {
   const int lane = threadIdx.x & 31;
-  const int d8 = d / 8;
-  const uint4* hsrc = reinterpret_cast<const uint4*>(Ht);
-  if (hs) {
-    for (int c = lane; c < d8; c += 32) hs[c] = __ldg(hsrc + c);
-    __syncwarp();
-  }
   bool ok = true;
-  for (int k0 = 0; k0 < K; k0 += ZU) {
-    const uint4* wr[ZU];
-    bool use[ZU];
-    float acc[ZU];
-#pragma unroll
-    for (int u = 0; u < ZU; ++u) {
-      const int k = k0 + u;
-      const int id = k < K ? __ldg(irow + k) : 0;  // same address in every lane
-      const bool in_range = id >= 0 && id < V;
-      ok = ok && (k >= K || in_range);
-      use[u] = k < K && in_range;
-      wr[u] = reinterpret_cast<const uint4*>(W + (long long)(use[u] ? id : 0) * d);
-      acc[u] = 0.f;
-    }
-    for (int c = lane; c < d8; c += 32) {
-      const uint4 h = hs ? hs[c] : __ldg(hsrc + c);
-#pragma unroll
-      for (int u = 0; u < ZU; ++u) acc[u] = dot8_bf16(h, __ldg(wr[u] + c), acc[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < ZU; ++u) {
-      const float z = warp_sum_f(acc[u]);
-      if (lane == 0 && k0 + u < K) zs[k0 + u] = use[u] ? z : 0.f;
-    }
+  for (int k = lane; k < K; k += 32) {
+    const int id = __ldg(irow + k);
+    ok = ok && id >= 0 && id < V;
+    zs[k] = __ldg(zrow + k);
   }
+  ok = __all_sync(0xffffffffu, ok);
   if (!ok && lane == 0) record_error(status, DEV_ERR_INDEX_RANGE);
   __syncwarp();
   return ok;
@@ -200,12 +168,11 @@ __device__ float rkl_token(const float* __restrict__ lrow, int K, float inv_tau,
   return warp_sum_f(r);
 }
 
-// Shared memory one warp of rkl_forward uses: z and log p (K floats each,
-// padded to 16 bytes) and, when H is staged, the d bf16 of the token's row.
-__host__ __device__ __forceinline__ size_t rkl_forward_smem_per_warp(int d, int K, bool stage_h) {
-  return (size_t)((K + 3) & ~3) * 8 + (stage_h ? (size_t)d * 2 : 0);
+// Shared memory one warp of rkl_forward uses: z and log p for the K ids
+// (K floats each, padded to 16 bytes).
+__host__ __device__ __forceinline__ size_t rkl_forward_smem_per_warp(int K) {
+  return (size_t)((K + 3) & ~3) * 8;
 }
-constexpr int RKL_STAGE_H_MAX_D = 8192;  // above this H is read from global memory
 
 // Counts the tokens that contribute.
 __global__ void rkl_count_kernel(const uint8_t* __restrict__ mask, int T, int* n_count) {
@@ -216,19 +183,17 @@ __global__ void rkl_count_kernel(const uint8_t* __restrict__ mask, int T, int* n
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(n_count, c);
 }
 
-// One warp per token. token_rkl, G and block_sums may each be null.
+// One warp per token, with z from zbuf (the segment kernel's output).
+// token_rkl, G and block_sums may each be null.
 //   G[t,k] = m_t / N * qt_k (log qt_k - log p_k - RKL_t) / tau   (0 off the support,
 //            for masked tokens, and for a token with an out-of-range id)
 //   block_sums[b] = sum over the block's unmasked tokens of RKL_t (fp64).
-// Dynamic shared memory per warp (rkl_forward_smem_per_warp): z and log p for
-// the K ids, then (STAGE_H) the token's row of H.
-template <bool STAGE_H>
 __global__ void __launch_bounds__(RKL_WARPS * 32)
-    rkl_forward_kernel(const uint16_t* __restrict__ H, const uint16_t* __restrict__ W,
-                       const int32_t* __restrict__ idx, const float* __restrict__ logit,
-                       const uint8_t* __restrict__ mask, int T, int d, int K, int V, float inv_tau,
-                       const int* __restrict__ n_count, float* __restrict__ token_rkl,
-                       float* __restrict__ G, double* __restrict__ block_sums, int* status) {
+    rkl_forward_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logit,
+                       const uint8_t* __restrict__ mask, int T, int K, int V, float inv_tau,
+                       const int* __restrict__ n_count, const float* __restrict__ zbuf,
+                       float* __restrict__ token_rkl, float* __restrict__ G,
+                       double* __restrict__ block_sums, int* status) {
   extern __shared__ __align__(16) unsigned char rkl_smem[];
   __shared__ double wsum[RKL_WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -236,12 +201,10 @@ __global__ void __launch_bounds__(RKL_WARPS * 32)
   double contrib = 0.0;
   if (t < T) {
     const int kpad = (K + 3) & ~3;
-    unsigned char* mine = rkl_smem + (size_t)warp * rkl_forward_smem_per_warp(d, K, STAGE_H);
-    float* zs = reinterpret_cast<float*>(mine);
+    float* zs = reinterpret_cast<float*>(rkl_smem + (size_t)warp * rkl_forward_smem_per_warp(K));
     float* ls = zs + kpad;
-    uint4* hs = STAGE_H ? reinterpret_cast<uint4*>(ls + kpad) : nullptr;
     const int32_t* irow = idx + (long long)t * K;
-    const bool ids_ok = rkl_gather_logits(H + (long long)t * d, hs, W, irow, d, K, V, zs, status);
+    const bool ids_ok = rkl_load_logits(irow, zbuf + (long long)t * K, K, V, zs, status);
     const float r = rkl_token(logit + (long long)t * K, K, inv_tau, zs, ls, status);
   const bool counted = mask == nullptr || mask[t] != 0;
     if (lane == 0) {
@@ -526,6 +489,78 @@ __device__ __forceinline__ void dW_flush(const float (&acc)[32], int v, int s, i
   }
 }
 
+// z for every (token, id) pair, vocabulary-major: one warp per segment of SEG
+// sorted pairs. For each run of equal id the warp holds that row of W (a
+// 1024-column slice per pass, in registers) and reads the rows of H of the
+// run's tokens, RB per memory round trip; each pair's dot product is summed
+// over the warp into shared memory, pass after pass. So every named row of W
+// is read once per segment it appears in, and the per-pair traffic is rows of
+// H (far smaller than W, mostly L2-resident). Pairs with an out-of-range id
+// (sorted to the bucket V) get z = 0.
+__global__ void __launch_bounds__(RKL_WARPS * 32)
+    rkl_z_segment_kernel(const uint16_t* __restrict__ H, const uint16_t* __restrict__ W,
+                         const int32_t* __restrict__ keys, const int32_t* __restrict__ vals,
+                         int n, int d, int K, int V, float* __restrict__ zbuf) {
+  __shared__ float zacc_all[RKL_WARPS][SEG];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x * RKL_WARPS + warp;
+  const int s0 = s * SEG;
+  if (s0 >= n) return;  // no block-wide barrier below
+  const int s1 = min(n, s0 + SEG);
+  float* zacc = zacc_all[warp];
+  for (int i = lane; i < SEG; i += 32) zacc[i] = 0.f;
+  __syncwarp();
+  for (int c0 = 0; c0 < d; c0 += 1024) {
+    bool col_ok[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) col_ok[q] = c0 + q * 256 + lane * 8 < d;
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+      const int i = i0 + lane;
+      const int cnt = min(32, s1 - i0);
+      const int my_v = i < s1 ? __ldg(keys + i) : -1;
+      const int my_t = i < s1 ? __ldg(vals + i) / K : 0;
+      const int prev_v = __shfl_up_sync(0xffffffffu, my_v, 1);
+      const unsigned starts = __ballot_sync(0xffffffffu, lane < cnt && (lane == 0 || my_v != prev_v));
+      for (int j = 0; j < cnt;) {  // one run of equal id per iteration (warp-uniform)
+        const int v = __shfl_sync(0xffffffffu, my_v, j);
+        const unsigned later = j < 31 ? starts & ~((2u << j) - 1u) : 0u;
+        const int jend = later ? __ffs(later) - 1 : cnt;
+        if (v < V) {
+          uint4 wv[4];
+          const uint16_t* wr = W + (long long)v * d;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = c0 + q * 256 + lane * 8;
+            wv[q] = __ldg(reinterpret_cast<const uint4*>(wr + (c < d ? c : 0)));
+          }
+          for (int jj = j; jj < jend; jj += RB) {
+            int row[RB];
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+              const int p = jj + u;
+              const int t = __shfl_sync(0xffffffffu, my_t, p & 31);
+              row[u] = p < jend ? t : 0;
+            }
+            uint4 h[RB][4];
+            load_slices(h, H, row, c0, d, lane);
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+              float a = 0.f;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) a = col_ok[q] ? dot8_bf16(h[u][q], wv[q], a) : a;
+              a = warp_sum_f(a);
+              if (lane == 0 && jj + u < jend) zacc[i0 - s0 + jj + u] += a;
+            }
+          }
+        }
+        j = jend;
+      }
+    }
+  }
+  __syncwarp();
+  for (int i = s0 + lane; i < s1; i += 32) zbuf[__ldg(vals + i)] = zacc[i - s0];
+}
+
 // One warp per segment of SEG sorted pairs. Pairs are taken 32 at a time
 // (one per lane), split into runs of equal id; each run is summed RB pairs per
 // memory round trip, and the sum is flushed when the id changes.
@@ -646,8 +681,9 @@ RklLayout rkl_layout(long long T, long long d, int K, long long V, size_t header
   size_t o = header;
   L.off_bsum = o;
   o += al256((size_t)((T + RKL_WARPS - 1) / RKL_WARPS) * sizeof(double));
-  L.fwd_total = o;
   L.off_G = o;
+  o += al256((size_t)L.n * 4);
+  L.off_z = o;
   o += al256((size_t)L.n * 4);
   for (int b = 0; b < 2; ++b) {
     L.off_keys[b] = o;
@@ -678,78 +714,23 @@ static int blocks_for(long long items, int per_block) {
   return (int)((items + per_block - 1) / per_block);
 }
 
-// rkl_forward_kernel with H staged in shared memory when d allows it.
-static cudaError_t launch_forward_kernel(const char* name, const uint16_t* H, const uint16_t* W,
-                                         const int32_t* idx, const float* logit,
-                                         const uint8_t* mask, int T, int d, int K, int V,
-                                         float inv_tau, const int* n_count, float* token_rkl,
+static cudaError_t launch_forward_kernel(const char* name, const int32_t* idx, const float* logit,
+                                         const uint8_t* mask, int T, int K, int V, float inv_tau,
+                                         const int* n_count, const float* zbuf, float* token_rkl,
                                          float* G, double* bsum, int* status,
                                          cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  // Largest dynamic shared memory set so far, per instantiation and device.
-  // The attribute is raised under a lock so that a smaller concurrent request
-  // cannot land after a larger one.
-  static std::atomic<size_t> attr_bytes[2][kMaxDevices] = {};
-  static std::mutex attr_mu;
-  const bool stage = d <= RKL_STAGE_H_MAX_D;
-  const size_t smem = RKL_WARPS * rkl_forward_smem_per_warp(d, K, stage);
-  void (*kern)(const uint16_t*, const uint16_t*, const int32_t*, const float*, const uint8_t*, int,
-               int, int, int, float, const int*, float*, float*, double*, int*) =
-      stage ? rkl_forward_kernel<true> : rkl_forward_kernel<false>;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::atomic<size_t>& set = attr_bytes[stage][dev];
-  if (smem > set.load(std::memory_order_acquire)) {
-    std::lock_guard<std::mutex> lk(attr_mu);
-    if (smem > set.load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      set.store(smem, std::memory_order_release);
-    }
-  }
-  return launch_kernel(name, kern, dim3(blocks_for(T, RKL_WARPS)), dim3(RKL_WARPS * 32), smem,
-                       stream, H, W, idx, logit, mask, T, d, K, V, inv_tau, n_count, token_rkl, G,
-                       bsum, status);
+  // at most 8 warps x 512 ids x 8 bytes = 32 KB: within the default limit
+  const size_t smem = RKL_WARPS * rkl_forward_smem_per_warp(K);
+  return launch_kernel(name, rkl_forward_kernel, dim3(blocks_for(T, RKL_WARPS)),
+                       dim3(RKL_WARPS * 32), smem, stream, idx, logit, mask, T, K, V, inv_tau,
+                       n_count, zbuf, token_rkl, G, bsum, status);
 }
 
-cudaError_t rkl_forward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
-                        const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
-                        int K, int V, float inv_tau, float* token_rkl, float* grad_z, float* loss,
-                        void* ws, int* status, int* n_count, int num_sms, cudaStream_t stream) {
-  cudaError_t e = launch_kernel("rkl_count", rkl_count_kernel, dim3(std::min(num_sms, 64)),
-                                dim3(256), 0, stream, mask, T, n_count);
-  if (e != cudaSuccess) return e;
-  double* bsum = ws_at<double>(ws, L.off_bsum);
-  e = launch_forward_kernel("rkl_forward", H, W, idx, logit, mask, T, d, K, V, inv_tau, n_count,
-                            token_rkl, grad_z, bsum, status, stream);
-  if (e != cudaSuccess) return e;
-  return launch_loss_finalize(bsum, blocks_for(T, RKL_WARPS), n_count, loss, stream);
-}
-
-cudaError_t rkl_backward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
-                         const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
-                         int K, int V, float inv_tau, const float* grad_z, float grad_loss,
-                         uint16_t* dH, float* dW, int accumulate, void* ws, int* status,
-                         int* n_count, int num_sms, cudaStream_t stream) {
+// Stable sort of the (id, position) pairs by id and each id's range in the
+// sorted list. *keys / *vals receive the sorted arrays (in the workspace).
+static cudaError_t rkl_sort(const RklLayout& L, const int32_t* idx, int V, void* ws, int num_sms,
+                            cudaStream_t stream, const int32_t** keys, const int32_t** vals) {
   cudaError_t e;
-  const float* G = grad_z;
-  if (G == nullptr) {  // recompute dL/dz at the ids
-    float* Gw = ws_at<float>(ws, L.off_G);
-    e = launch_kernel("rkl_count", rkl_count_kernel, dim3(std::min(num_sms, 64)), dim3(256), 0,
-                      stream, mask, T, n_count);
-    if (e != cudaSuccess) return e;
-    e = launch_forward_kernel("rkl_grad", H, W, idx, logit, mask, T, d, K, V, inv_tau, n_count,
-                              nullptr, Gw, nullptr, status, stream);
-    if (e != cudaSuccess) return e;
-    G = Gw;
-  }
-  e = launch_kernel("rkl_dH", rkl_dH_kernel, dim3(blocks_for(T, RKL_WARPS)), dim3(RKL_WARPS * 32),
-                    0, stream, W, idx, G, grad_loss, T, d, K, V, dH, status);
-  if (e != cudaSuccess) return e;
-
-  // sort the (id, position) pairs by id, stably
   const int n = (int)L.n;
   unsigned* hist = ws_at<unsigned>(ws, L.off_hist);
   const int32_t* kin = idx;
@@ -792,15 +773,74 @@ cudaError_t rkl_backward(const RklLayout& L, const uint16_t* H, const uint16_t* 
                     dim3(std::max(1, std::min(num_sms * 8, blocks_for(n, 256)))), dim3(256), 0,
                     stream, kin, n, bstart, bend);
   if (e != cudaSuccess) return e;
+  *keys = kin;
+  *vals = vin;
+  return cudaSuccess;
+}
+
+// count -> sort -> z per pair (segments) -> per-token RKL / grad_z / block sums.
+static cudaError_t rkl_token_pass(const RklLayout& L, const uint16_t* H, const uint16_t* W,
+                                  const int32_t* idx, const float* logit, const uint8_t* mask,
+                                  int T, int d, int K, int V, float inv_tau, float* token_rkl,
+                                  float* G, double* bsum, void* ws, int* status, int* n_count,
+                                  int num_sms, cudaStream_t stream, const int32_t** keys,
+                                  const int32_t** vals) {
+  cudaError_t e = launch_kernel("rkl_count", rkl_count_kernel, dim3(std::min(num_sms, 64)),
+                                dim3(256), 0, stream, mask, T, n_count);
+  if (e != cudaSuccess) return e;
+  if ((e = rkl_sort(L, idx, V, ws, num_sms, stream, keys, vals)) != cudaSuccess) return e;
+  float* zbuf = ws_at<float>(ws, L.off_z);
+  e = launch_kernel("rkl_z_segment", rkl_z_segment_kernel, dim3(blocks_for(L.n_seg, RKL_WARPS)),
+                    dim3(RKL_WARPS * 32), 0, stream, H, W, *keys, *vals, (int)L.n, d, K, V, zbuf);
+  if (e != cudaSuccess) return e;
+  return launch_forward_kernel("rkl_forward", idx, logit, mask, T, K, V, inv_tau, n_count, zbuf,
+                               token_rkl, G, bsum, status, stream);
+}
+
+cudaError_t rkl_forward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
+                        const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
+                        int K, int V, float inv_tau, float* token_rkl, float* grad_z, float* loss,
+                        void* ws, int* status, int* n_count, int num_sms, cudaStream_t stream) {
+  double* bsum = ws_at<double>(ws, L.off_bsum);
+  const int32_t* keys = nullptr;
+  const int32_t* vals = nullptr;
+  cudaError_t e = rkl_token_pass(L, H, W, idx, logit, mask, T, d, K, V, inv_tau, token_rkl, grad_z,
+                                 bsum, ws, status, n_count, num_sms, stream, &keys, &vals);
+  if (e != cudaSuccess) return e;
+  return launch_loss_finalize(bsum, blocks_for(T, RKL_WARPS), n_count, loss, stream);
+}
+
+cudaError_t rkl_backward(const RklLayout& L, const uint16_t* H, const uint16_t* W,
+                         const int32_t* idx, const float* logit, const uint8_t* mask, int T, int d,
+                         int K, int V, float inv_tau, const float* grad_z, float grad_loss,
+                         uint16_t* dH, float* dW, int accumulate, void* ws, int* status,
+                         int* n_count, int num_sms, cudaStream_t stream) {
+  cudaError_t e;
+  const int32_t* keys = nullptr;
+  const int32_t* vals = nullptr;
+  const float* G = grad_z;
+  if (G == nullptr) {  // recompute dL/dz at the ids (the sort is reused for dW)
+    float* Gw = ws_at<float>(ws, L.off_G);
+    e = rkl_token_pass(L, H, W, idx, logit, mask, T, d, K, V, inv_tau, nullptr, Gw, nullptr, ws,
+                       status, n_count, num_sms, stream, &keys, &vals);
+    if (e != cudaSuccess) return e;
+    G = Gw;
+  } else if ((e = rkl_sort(L, idx, V, ws, num_sms, stream, &keys, &vals)) != cudaSuccess) {
+    return e;
+  }
+  e = launch_kernel("rkl_dH", rkl_dH_kernel, dim3(blocks_for(T, RKL_WARPS)), dim3(RKL_WARPS * 32),
+                    0, stream, W, idx, G, grad_loss, T, d, K, V, dH, status);
+  if (e != cudaSuccess) return e;
+  const int* bstart = ws_at<int>(ws, L.off_bstart);
+  const int* bend = ws_at<int>(ws, L.off_bend);
   float* part = ws_at<float>(ws, L.off_part);
   e = launch_kernel("rkl_dW_segment", rkl_dW_segment_kernel,
-                    dim3(blocks_for(L.n_seg, RKL_WARPS)), dim3(RKL_WARPS * 32), 0, stream, H, kin,
-                    vin, G, grad_loss, (const int*)bstart, (const int*)bend, n, d, K, V, dW, part,
-                    accumulate);
+                    dim3(blocks_for(L.n_seg, RKL_WARPS)), dim3(RKL_WARPS * 32), 0, stream, H, keys,
+                    vals, G, grad_loss, bstart, bend, (int)L.n, d, K, V, dW, part, accumulate);
   if (e != cudaSuccess) return e;
   return launch_kernel("rkl_dW_fixup", rkl_dW_fixup_kernel, dim3(blocks_for(V, RKL_WARPS)),
-                       dim3(RKL_WARPS * 32), 0, stream, (const int*)bstart, (const int*)bend,
-                       (const float*)part, V, d, dW, accumulate);
+                       dim3(RKL_WARPS * 32), 0, stream, bstart, bend, (const float*)part, V, d, dW,
+                       accumulate);
 }
 
 }  // namespace kdkl

@@ -152,12 +152,12 @@ def test_rkl_pointer_errors_and_workspace(lib):
     assert _rkl_bwd(lib, p, dW=0) == 1
     assert _rkl_bwd(lib, p, dH=24) == 3
     assert _rkl_bwd(lib, p, g=float("inf")) == 1
-    # linear in T (no T x V term): per pair the gradient, two sort buffers and
+    # linear in T (no T x V term): per pair the gradient, z, two sort buffers and
     # the dW partials (2 rows of d fp32 per 256 pairs); 8 bytes per vocabulary row
     T, d, V, K = 32768, 2880, 201088, 100
     sizes = [kdkl.kd_rkl_workspace_size(t, d, V, K) for t in (T // 4, T // 2, T)]
     assert sizes[0] < sizes[1] < sizes[2]
-    per_pair = 4 * 5 + 2 * d * 4 / 256 + 1  # + radix histograms (<= 1 byte per pair)
+    per_pair = 4 * 6 + 2 * d * 4 / 256 + 1  # + radix histograms (<= 1 byte per pair)
     assert sizes[2] <= T * K * per_pair + 8 * (V + 1) + T + (1 << 20)
     assert abs((sizes[2] - sizes[1]) - (sizes[1] - sizes[0]) * 2) < (1 << 20)
     # T * K must stay below 2^31

@@ -210,3 +210,22 @@ def test_full_size_sparse_mask(kdkl, name):
     keep_v = torch.zeros(w.V, dtype=torch.bool, device="cuda")
     keep_v[t_dev] = True
     assert torch.count_nonzero(dW[~keep_v]).item() == 0
+
+
+def test_null_mask_equals_all_ones(kdkl):
+    """mask = NULL counts every token: the same bits as an all-ones mask."""
+    w = WORKLOADS["small"].with_(T=150, d=96, V=900, K=11, tau=1.2)
+    x = make_inputs(w, seed=29)
+    g = {k: v.cuda() for k, v in x.items()}
+    ones = torch.ones(w.T, dtype=torch.uint8, device="cuda")
+    out = []
+    for m in (None, ones):
+        loss, tok, gz = kdkl.kd_rkl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], m,
+                                            temperature=w.tau, want_token_rkl=True,
+                                            want_grad_z=True)
+        dH, dW = kdkl.kd_rkl_backward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], m,
+                                      temperature=w.tau, grad_z=gz)
+        out.append((loss, tok, gz, dH, dW))
+    torch.cuda.synchronize()
+    for a, b in zip(*out):
+        assert torch.equal(a, b)

@@ -128,3 +128,11 @@ def test_gptoss_full_size_sampled_rows(kdkl):
                                      np.random.default_rng(1).choice(T, 40, replace=False)]))
     exact = check_rows(ids, vals, H64, W64, 100, rows)
     assert exact >= 0.8 * len(rows)
+
+
+def test_empty_input(kdkl):
+    H = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda")
+    idx, val = kdkl.kd_lmhead_topk(H, W, 10)
+    torch.cuda.synchronize()
+    assert idx.shape == (0, 10) and val.shape == (0, 10)

@@ -232,6 +232,68 @@ __device__ __forceinline__ uint32_t merge_order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Number of keys among keys[0, m) at or below x, summed over the warp.
+__device__ __forceinline__ int merge_count_le(const unsigned long long* keys, int m,
+                                              unsigned long long x) {
+  int c = 0;
+  for (int i = threadIdx.x & 31; i < m; i += 32) c += keys[i] <= x ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
+
+// Moves the K smallest of keys[0, m) (all distinct: the low half is the id)
+// to keys[0, K), in their original order, and returns K. The K-th smallest key
+// is found by bisection, first over the high 32 bits (the logit order), then,
+// only when several entries share the K-th logit, over the low 32 bits (the
+// id), so that ties keep the smaller ids.
+__device__ int merge_select_k(unsigned long long* keys, int m, int K) {
+  const int lane = threadIdx.x & 31;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i = lane; i < m; i += 32) {
+    const uint32_t h = (uint32_t)(keys[i] >> 32);
+    lo = min(lo, h);
+    hi = max(hi, h);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  while (lo < hi) {  // smallest h with at least K keys whose high half is <= h
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    if (merge_count_le(keys, m, ((unsigned long long)mid << 32) | 0xffffffffull) >= K)
+      hi = mid;
+    else
+      lo = mid + 1u;
+  }
+  unsigned long long cut = ((unsigned long long)lo << 32) | 0xffffffffull;
+  if (merge_count_le(keys, m, cut) > K) {  // ties on the K-th logit: bisect the ids
+    uint32_t a = 0u, b = 0xffffffffu;
+    while (a < b) {
+      const uint32_t mid = a + ((b - a) >> 1);
+      if (merge_count_le(keys, m, ((unsigned long long)lo << 32) | mid) >= K)
+        b = mid;
+      else
+        a = mid + 1u;
+    }
+    cut = ((unsigned long long)lo << 32) | a;
+  }
+  // stable in-place compaction of the keys <= cut (exactly K of them)
+  const uint32_t below = (1u << lane) - 1u;
+  int w = 0;
+  for (int i0 = 0; i0 < m; i0 += 32) {
+    const int i = i0 + lane;
+    const unsigned long long k = i < m ? keys[i] : ~0ull;
+    const bool keep = i < m && k <= cut;
+    const uint32_t mask = __ballot_sync(0xffffffffu, keep);  // all reads of this round are done
+    if (keep) keys[w + __popc(mask & below)] = k;
+    w += __popc(mask);
+  }
+  __syncwarp();
+  return w;
+}
+
 // One warp per row; `rows_per_block` warps share the block's shared memory,
 // cap entries (a power of two >= nsplit * K) each.
 __global__ void __launch_bounds__(256)
@@ -273,6 +335,8 @@ __global__ void __launch_bounds__(256)
       m += __popc(mask);
     }
   }
+  __syncwarp();
+  if (m > K) m = merge_select_k(mkeys, m, K);  // keep the K best, then sort only those
   int p2 = 2;
   while (p2 < m) p2 <<= 1;
   for (int e = m + lane; e < p2; e += 32) mkeys[e] = ~0ull;

@@ -136,3 +136,19 @@ def test_empty_input(kdkl):
     idx, val = kdkl.kd_lmhead_topk(H, W, 10)
     torch.cuda.synchronize()
     assert idx.shape == (0, 10) and val.shape == (0, 10)
+
+
+@pytest.mark.parametrize("V,K", [(3000, 100), (40000, 256), (700, 7)])
+def test_exact_ties_keep_smaller_ids(kdkl, V, K):
+    """Every row of W identical: all logits of a row tie, so the top-K is the
+    K smallest ids in increasing order (ties go to the smaller id in the
+    epilogue compaction, the merge's selection and the final sort alike)."""
+    T, d = 300, 64
+    g = torch.Generator().manual_seed(3)
+    H = torch.randn(T, d, generator=g).to(torch.bfloat16).cuda()
+    W = torch.randn(1, d, generator=g).to(torch.bfloat16).repeat(V, 1).cuda()
+    idx, val = kdkl.kd_lmhead_topk(H, W, K)
+    torch.cuda.synchronize()
+    want = torch.arange(K, dtype=torch.int32, device="cuda").expand(T, K)
+    assert torch.equal(idx, want)
+    assert torch.equal(val, val[:, :1].expand(T, K))  # one logit per row

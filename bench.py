@@ -17,6 +17,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -47,12 +48,20 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments, blank lines or trailing spaces, so that a
+    comment edit does not invalidate counters taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def csrc_digest() -> str:
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "lm_head_top_gb300", "csrc")
     for name in sorted(os.listdir(cdir)):
-        with open(os.path.join(cdir, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(cdir, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -181,7 +181,8 @@ kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, co
  *   grad_z[t,k] = dloss/dz[t,idx[t,k]] = m[t]/N * qt (log qt - log p - RKL[t]) / tau
  *               (0 for dropped entries)
  * Only the K cached logits of each token enter, so there is no vocabulary-wide
- * contraction: the kernels gather rows of W (CUDA cores). The problem struct
+ * contraction: the kernels stream rows of W and H per (token, id) pair, on CUDA
+ * cores, over the pairs sorted by id (forward, dW) or per token (dH). The problem struct
  * is kd_kl_problem; `chunk` is not used (any value >= 1); T * K < 2^31.
  * Both calls take a workspace of kd_rkl_workspace_size() bytes: linear in T,
  * plus 8 bytes per vocabulary row. */
@@ -200,7 +201,7 @@ kd_status kd_rkl_forward(const kd_kl_problem* prob, const uint16_t* H, const uin
 
 /* Gradients of grad_loss * loss.
  *   grad_z  [T, K] fp32 or NULL   from kd_rkl_forward on the same inputs; NULL:
- *                                 the backward recomputes it (one more gather of W)
+ *                                 the backward recomputes it (the forward's z pass)
  *   dH      [T, d] bf16 out       overwritten (fp32 sums inside; masked rows = 0)
  *   dW      [V, d] fp32 out       overwritten, or added to when accumulate_dW != 0
  * The (id, token) pairs are sorted by id inside the call so that each dW row is

@@ -116,7 +116,7 @@ enum GemmKind {
 // (0 if unknown). The persistent grid must not exceed it.
 int pair_max_active_clusters();
 
-// bn: N tile width (LOGIT_BN for the logit GEMMs; 256 or 192 for dH/dW).
+// bn: N tile width (LOGIT_BN for the logit GEMMs; 256 for dH/dW).
 // pair: 2-CTA clusters sharing one 256 x bn tile (grid must be even).
 cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA,
                         const CUtensorMap& tmB,

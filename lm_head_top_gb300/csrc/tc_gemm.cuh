@@ -9,13 +9,17 @@
 //   EPI_GRAD  backward: recompute S, form (softmax - P) * m / (tau N) * g in
 //             the epilogue and store it as bf16 into the chunk buffer.
 //   EPI_STORE plain fp32 output (dH and dW GEMMs), store or add.
+//   EPI_TOPK  teacher cache producer: per-row candidate lists above a running
+//             admission threshold, compacted to the row's top-K per split.
+//   EPI_LSE_MIX / EPI_GRAD_MIX  the soft KL mixed with a hard-label CE.
 //
 // Roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
-// Tiles are 128 x BN (BN = 256, or 192 for the dH/dW GEMMs when the hidden
-// size is a multiple of 192 but not of 256) with a 64-deep K step, 4-5
-// shared-memory stages, and two fp32 accumulators in TMEM so the epilogue of
-// one tile overlaps the MMAs of the next.
+// By default two CTAs of a cluster share a 256 x 256 tile (tcgen05
+// cta_group::2; PAIR); otherwise tiles are 128 x BN. The K step is 64 deep,
+// with as many shared-memory stages as fit in ~200 KB (6 for pairs), and two
+// fp32 accumulators in TMEM so the epilogue of one tile overlaps the MMAs of
+// the next.
 //
 // Source of the method: "Efficient Knowledge Distillation for LLMs: Offline
 // Top-K Logits and a Fused Chunked KL Loss", page "Making knowledge

@@ -80,6 +80,10 @@ struct GemmShape {
   // warp's first wait runs out (after kInjectedWaitLimitNs) and the block
   // unwinds through its error path. Never set in normal calls.
   int inject_stall;
+  // When > 0, the first group holds only this many splits (the rest use
+  // group_n): the top-K producer runs one split of every row first, so that
+  // the row's other splits start from the threshold it publishes.
+  int first_group;
 };
 
 struct EpiParams {
@@ -233,12 +237,25 @@ __device__ __forceinline__ float topk_shared_threshold(const uint32_t* row_key) 
 
 __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
                                             int& ne) {
+  int s_base = 0;
+  if (sh.first_group > 0) {
+    const int fg_units = sh.m_tiles * sh.first_group;
+    if (u < fg_units) {
+      m = u / sh.first_group;
+      s = u - m * sh.first_group;
+      nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
+      ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
+      return;
+    }
+    u -= fg_units;
+    s_base = sh.first_group;
+  }
   const int per_group = sh.m_tiles * sh.group_n;
   const int g = u / per_group;
   const int r = u - g * per_group;
-  const int gsize = min(sh.group_n, sh.nsplit - g * sh.group_n);  // last group may be short
+  const int gsize = min(sh.group_n, sh.nsplit - s_base - g * sh.group_n);  // last may be short
   m = r / gsize;
-  s = g * sh.group_n + (r - m * gsize);
+  s = s_base + g * sh.group_n + (r - m * gsize);
   nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
   ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
 }

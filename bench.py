@@ -179,6 +179,40 @@ def oracle_arrays(x):
             x["mask"].numpy())
 
 
+def blas_threads() -> int:
+    """Threads the oracle's BLAS runs its products on: the library's own
+    count where it can be read, else the thread variables it honours, else
+    every core (the OpenBLAS default)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    try:  # the OpenBLAS numpy loaded, asked directly
+        import ctypes
+        with open("/proc/self/maps") as f:
+            libs = {ln.split()[-1] for ln in f if "openblas" in ln.lower() and ".so" in ln}
+        for lib in sorted(libs):
+            h = ctypes.CDLL(lib)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                        "openblas_get_num_threads"):
+                fn = getattr(h, sym, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    n = int(fn())
+                    if n > 0:
+                        return n
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(k, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    return os.cpu_count() or 1
+
+
 def time_oracle(x_np, w, n_tokens: int, repeats: int = 1):
     rng = np.random.default_rng(0)
     times = []
@@ -359,7 +393,7 @@ def run_kdkl(args):
             x_np = oracle_arrays(x)
             n_cpu = args.cpu_tokens
             t = time_oracle(x_np, w, n_cpu)[0]
-            cpu = {"value": round(n_cpu / t, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+            cpu = {"value": round(n_cpu / t, 3), "unit": "tokens/s", "cores": blas_threads(),
                    "kind": "oracle",
                    "sample": "fp64 oracle forward+backward on %d random tokens of %s (all V=%d, "
                              "d=%d; dense logits row blocks), %.1f s" % (min(n_cpu, T), wname, V,
@@ -585,7 +619,7 @@ def run_reference(args):
     times = time_oracle(x_np, w, n, repeats=args.steps)
     total = sum(times)
     value = n * args.steps / total
-    cpu = {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    cpu = {"value": round(value, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
            "sample": "fp64 oracle forward+backward on %d random tokens of %s per step "
                      "(all V=%d, d=%d)" % (n, WORKLOAD, w.V, w.d)}
     return {

@@ -159,3 +159,58 @@ def test_timing_and_launch_count(kdkl):
             "dH_gemm", "dW_gemm", "f32_to_bf16"} <= names
     assert kdkl.kd_launch_count() - before == sum(r[1] for r in rows)
     assert all(r[2] > 0 for r in rows)
+
+
+def test_teacher_edge_entries(kdkl):
+    """-inf teacher logits (p = 0, outside the support), ids repeated within a
+    row (entries add: reading 6) and a row whose support is one entry, across
+    several token chunks and vocabulary slabs."""
+    w = WORKLOADS["small"].with_(T=96, d=64, V=500, K=12, chunk=32, tau=1.3)
+    x = make_inputs(w, seed=11)
+    lg, idx = x["topk_logit"], x["topk_idx"]
+    lg[3, 5:] = float("-inf")            # half the row outside the support
+    idx[7, 4] = idx[7, 2]                # a repeated id
+    lg[9, 1:] = float("-inf")            # a single-entry support
+    idx[11, 1] = idx[11, 0]              # repeat, and the repeat dropped
+    lg[11, 1] = float("-inf")
+    idx[40, :] = idx[40, 0]              # one id named K times
+    _compare(run_gpu(kdkl, x, w.tau, w.chunk, grad_loss=0.5), x, w.tau, grad_loss=0.5)
+
+
+def test_large_logits(kdkl):
+    """Logits of a few hundred at a sharp temperature: the online
+    logsumexp must not overflow, and the loss stays exact."""
+    w = WORKLOADS["small"].with_(T=160, d=96, V=1500, K=16, chunk=64, tau=0.5)
+    x = make_inputs(w, seed=12)
+    x["H"] = (x["H"].float() * 60.0).to(torch.bfloat16)   # z ~ N(0, 60^2)
+    x["topk_logit"] = x["topk_logit"] * 40.0
+    out = run_gpu(kdkl, x, w.tau, w.chunk)
+    assert np.isfinite(out["loss"]) and np.isfinite(out["lse"]).all()
+    _compare(out, x, w.tau)
+
+
+@pytest.mark.parametrize("bad", ["all_neg_inf", "nan", "pos_inf"])
+def test_unusable_teacher_row_is_reported(kdkl, bad):
+    """A teacher row with no finite logit, a NaN or +inf is an invalid input:
+    the device status says KD_ERR_INVALID_ARG (1); a clean call afterwards on
+    the same workspace reports 0."""
+    w = WORKLOADS["small"].with_(T=64, d=16, V=100, K=3, chunk=16)
+    x = make_inputs(w, seed=13)
+    row = x["topk_logit"][9]
+    if bad == "all_neg_inf":
+        row[:] = float("-inf")
+    elif bad == "nan":
+        row[1] = float("nan")
+    else:
+        row[0] = float("inf")
+    g = {k: v.cuda() for k, v in x.items()}
+    ws = torch.empty(kdkl.kd_kl_workspace_size(64, 16, 100, 3, 1.0, 16, 0), dtype=torch.uint8,
+                     device="cuda")
+    kdkl.kd_kl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], chunk=16,
+                       workspace=ws)
+    assert kdkl.kd_kl_check_status(ws) == 1
+    clean = make_inputs(w, seed=13)
+    g = {k: v.cuda() for k, v in clean.items()}
+    kdkl.kd_kl_forward(g["H"], g["W"], g["topk_idx"], g["topk_logit"], g["mask"], chunk=16,
+                       workspace=ws)
+    assert kdkl.kd_kl_check_status(ws) == 0

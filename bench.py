@@ -171,6 +171,38 @@ def oracle_sample_step(x_np, w, rows, block: int = 1024):
         ok.backward(Hs, W, idxs, lgs, ms, w.tau, 1.0)
 
 
+def oracle_rkl_sample_step(x_np, w, rows, block: int = 1024):
+    """fp64 oracle reverse-KL forward + backward on a sample of token rows."""
+    import oracle.kl_oracle as ok
+    H, W, idx, logit, mask = x_np
+    for b in range(0, len(rows), block):
+        r = rows[b:b + block]
+        ok.reverse_kl_forward(H[r], W, idx[r], logit[r], mask[r], w.tau)
+        ok.reverse_kl_backward(H[r], W, idx[r], logit[r], mask[r], w.tau, 1.0)
+
+
+def oracle_topk_sample_step(x_np, w, rows, K: int = 100, block: int = 512):
+    """fp64 oracle top-K (dense row of logits, then the ordered K largest) on
+    a sample of token rows."""
+    import oracle.kl_oracle as ok
+    H, W = x_np[0], x_np[1]
+    for b in range(0, len(rows), block):
+        ok.topk_logits(H[rows[b:b + block]], W, K)
+
+
+def cpu_baseline(step_fn, x_np, w, n_tokens: int, what: str):
+    """Times step_fn (an oracle sample step) on n_tokens random rows of w."""
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
+    t0 = time.perf_counter()
+    step_fn(x_np, w, rows)
+    t = time.perf_counter() - t0
+    return {"value": round(len(rows) / t, 3), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": "fp64 oracle %s on %d random tokens of %s (all V=%d, d=%d), %.1f s"
+                      % (what, len(rows), w.name, w.V, w.d, t)}
+
+
 def oracle_arrays(x):
     import oracle.kl_oracle as ok
     return (ok.bf16_bits_to_f64(x["H"].view(torch.int16).numpy()),
@@ -482,8 +514,35 @@ def run_topk(args):
         per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    launches = kdkl.kd_launch_count() - launches0
+
+    # ---- end to end: pinned host H copied in, the cache (ids + logits) read back
+    e2e = None
+    if not args.no_e2e:
+        H_host = x["H"].pin_memory()
+        idx_host = torch.empty(T, K, dtype=torch.int32).pin_memory()
+        val_host = torch.empty(T, K, dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            H.copy_(H_host, non_blocking=True)
+            step()
+            idx_host.copy_(idx, non_blocking=True)
+            val_host.copy_(val, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": round(T * world * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * K * 8}
     if rank != 0:
         return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(oracle_topk_sample_step, oracle_arrays(x), w, args.cpu_tokens // 2,
+                           "top-%d (dense logit rows, ordered selection)" % K)
     pk, pk_src = peaks()
     rows = {n: (c, ms) for n, c, ms in per_kernel}
     c, ms = rows["topk_gemm"]
@@ -504,7 +563,9 @@ def run_topk(args):
                      "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
                      "peak_source": "%s bf16_tflops_sustained" % pk_src,
                      "traffic": recorded_traffic("topk_gemm", w.name if not args.tokens else "")},
-        "gpu_launches": kdkl.kd_launch_count() - launches0,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
         "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
         "clocks": clocks.summary(),
     }
@@ -561,8 +622,35 @@ def run_rkl(args):
         per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    launches = kdkl.kd_launch_count() - launches0
+
+    # ---- end to end: pinned host H and teacher cache copied in, loss read back
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.pin_memory() for k, v in x.items() if k != "W"}
+        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for k in host:
+                g[k].copy_(host[k], non_blocking=True)
+            step()
+            loss_host.copy_(loss, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": round(T * world * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4}
     if rank != 0:
         return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(oracle_rkl_sample_step, oracle_arrays(x), w, args.cpu_tokens,
+                           "reverse-KL forward+backward")
     pk, pk_src = peaks()
     # Algorithmic bytes per launch of each large kernel: every distinct W row
     # the cache names read once, H read once, the cache (ids, logits or the
@@ -598,7 +686,9 @@ def run_rkl(args):
                      "pair_gather_gbs": round(gather_gbs, 1),
                      "pair_gather_frac": round(gather_gbs / pk["hbm_gbs"], 4),
                      "traffic": recorded_traffic(dom, wname)},
-        "gpu_launches": kdkl.kd_launch_count() - launches0,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
         "kernel_ms_per_step": {n: round(v / args.steps, 3) for n, cc, v in per_kernel},
         "clocks": clocks.summary(),
     }

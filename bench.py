@@ -190,6 +190,17 @@ def oracle_topk_sample_step(x_np, w, rows, K: int = 100, block: int = 512):
         ok.topk_logits(H[rows[b:b + block]], W, K)
 
 
+def step_marks(n: int):
+    """One timing event per step, created before the timed loop."""
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def step_stats(ev0, marks):
+    """(median, min) ms of the individual steps between ev0 and the marks."""
+    ms = [ev0.elapsed_time(marks[0])] + [a.elapsed_time(b) for a, b in zip(marks, marks[1:])]
+    return round(float(np.median(ms)), 3), round(float(min(ms)), 3)
+
+
 def cpu_baseline(step_fn, x_np, w, n_tokens: int, what: str):
     """Times step_fn (an oracle sample step) on n_tokens random rows of w."""
     rng = np.random.default_rng(0)
@@ -329,15 +340,18 @@ def run_kdkl(args):
         barrier(world)
         torch.cuda.synchronize(dev)
         kdkl.kd_timing_begin()
+        marks = step_marks(args.steps)
         ev0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step(g)
+            marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         per_kernel = kdkl.kd_timing_end()
         barrier(world)
     launches = kdkl.kd_launch_count() - launches0
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     clk = clocks.summary()
     peak_hbm = torch.cuda.max_memory_allocated(dev) / 2 ** 30
 
@@ -438,6 +452,8 @@ def run_kdkl(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(elapsed_ms / args.steps, 3),
+            "ms_per_step_median": med_ms,
+            "ms_per_step_min": min_ms,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -506,14 +522,17 @@ def run_topk(args):
         barrier(world)
         torch.cuda.synchronize(dev)
         kdkl.kd_timing_begin()
+        marks = step_marks(args.steps)
         ev0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step()
+            marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     launches = kdkl.kd_launch_count() - launches0
 
     # ---- end to end: pinned host H copied in, the cache (ids + logits) read back
@@ -552,7 +571,8 @@ def run_topk(args):
         "metric": "offline top-K teacher cache (LM head x top-100) tokens/s", "path": "topk",
         "value": round(T * world * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
-        "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
+        "ms_per_step": round(elapsed_ms / args.steps, 3), "ms_per_step_median": med_ms,
+        "ms_per_step_min": min_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "%s_topk" % w.name, "T": T, "d": d, "V": V, "K": K,
                    "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
@@ -614,14 +634,17 @@ def run_rkl(args):
         barrier(world)
         torch.cuda.synchronize(dev)
         kdkl.kd_timing_begin()
+        marks = step_marks(args.steps)
         ev0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step()
+            marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     launches = kdkl.kd_launch_count() - launches0
 
     # ---- end to end: pinned host H and teacher cache copied in, loss read back
@@ -674,14 +697,16 @@ def run_rkl(args):
         "metric": "reverse KL over the cached ids fwd+bwd tokens/s", "path": "rkl",
         "value": round(T * world * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
+        "ms_per_step": round(elapsed_ms / args.steps, 3), "ms_per_step_median": med_ms,
+        "ms_per_step_min": min_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "%s_rkl" % wname,
                    "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "distinct_ids": distinct,
                    "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
         "peak_hbm_gib": round(torch.cuda.max_memory_allocated(dev) / 2 ** 30, 3),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4),
                      "peak_source": "%s hbm_gbs" % pk_src, "bytes_per_launch": algo,
                      "pair_gather_gbs": round(gather_gbs, 1),
                      "pair_gather_frac": round(gather_gbs / pk["hbm_gbs"], 4),

@@ -86,6 +86,19 @@ def check_full_mask(kdkl, w, x, g, Hn, Wn, idx, lg, chunk=None, n_rows=64, seed=
     # loss is the mean of the (device) per-token KL over the mask
     kl_all = run.kl.double().cpu().numpy()
     assert abs(run.loss.item() - kl_all[mask != 0].mean()) <= 1e-5 * abs(run.loss.item())
+    # Every row of G sums to zero over the vocabulary (q and P are both
+    # distributions), so the columns of dW = G^T H sum to zero: a check on
+    # every row of the full-size dW. What remains is the bf16 rounding of G
+    # (~1e-3 of |dW|); a dropped tile or slab leaves several per cent.
+    # Summed in fp64 over 256-row blocks: a few MB of temporaries.
+    colsum = torch.zeros(run.dW.shape[1], dtype=torch.float64, device=run.dW.device)
+    sq = torch.zeros((), dtype=torch.float64, device=run.dW.device)
+    for r0 in range(0, run.dW.shape[0], 256):
+        blk = run.dW[r0:r0 + 256].double()
+        colsum += blk.sum(0)
+        sq += (blk * blk).sum()
+        del blk
+    assert (torch.linalg.vector_norm(colsum) / sq.sqrt()).item() <= 1e-2
     return run
 
 

@@ -1,15 +1,15 @@
 /*
  * kdkl.h — C ABI of the fused chunked KL distillation loss for GB300 (sm_103a).
  *
- * The operation is the one stated in "Efficient Knowledge Distillation for
- * LLMs: Offline Top-K Logits and a Fused Chunked KL Loss" (page "Making
- * knowledge distillation cheap enough to run at scale", section "Two system
- * changes"): a student's output projection z = H W^T over the full
- * vocabulary, compared by a KL divergence with an offline cache of the
- * teacher's top-K (id, logit) pairs per token, without ever storing the
- * tokens x vocabulary logit grid. The backward recomputes the projection
- * (same section, the fused-chunked bullet; page 4, section "Two systemic
- * changes", item 2: "the backward pass recomputes each chunk on the fly").
+ * The operation is the one the pages state ("Making knowledge distillation
+ * cheap enough to run at scale", section "Two system changes"): a student's
+ * output projection z = H W^T over the full vocabulary, compared by a KL
+ * divergence with an offline cache of the teacher's top-K (id, logit) pairs
+ * per token, without ever storing the tokens x vocabulary logit grid. The
+ * backward computes each chunk's projection a second time instead of keeping
+ * it (same section, the fused-chunked bullet; "Efficient knowledge
+ * distillation for LLMs: offline top-K logits and a fused chunked KL loss",
+ * section "Two systemic changes for scalable distillation", item 2).
  *
  * Definitions (the pages name a closed-form gradient but do not print it):
  *   p[t,k]   = softmax_k(topk_logit[t,k] / tau)        teacher, renormalised over K

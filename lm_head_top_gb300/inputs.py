@@ -7,8 +7,9 @@ the tensors it returns, so a parity test compares the two on identical bytes.
 
 Workloads stand in for the pages' own runs ("Efficient Knowledge Distillation
 for LLMs: Offline Top-K Logits and a Fused Chunked KL Loss"): the 8K-context
-Llama-3.2-3B-like student (page 4, benchmark table), the GPT-OSS-20B run at
-32,768 tokens ("Scaling to long contexts"), and the toy output-projection
+Llama-3.2-3B-like student (that page's "Performance and memory benchmarks"
+table), the GPT-OSS-20B run at 32,768 tokens ("Scaling to long contexts"),
+and the toy output-projection
 benchmark that runs to 256K tokens. The real models, teacher caches and
 training data are not used: every tensor is synthetic.
 

@@ -6,10 +6,11 @@ library and its Python binding) never imports, calls or links anything here,
 and nothing here imports the product. Inputs reach both sides from the seeded
 generator, which holds none of this arithmetic.
 
-What it computes follows the pages' statement of the method ("Efficient
-Knowledge Distillation for LLMs: Offline Top-K Logits and a Fused Chunked KL
-Loss"; page "Making knowledge distillation cheap enough to run at scale",
-section "Two system changes"):
+What it computes follows the pages' statement of the method ("Making
+knowledge distillation cheap enough to run at scale", section "Two system
+changes"; the same method in "Efficient knowledge distillation for LLMs:
+offline top-K logits and a fused chunked KL loss", section "Two systemic
+changes for scalable distillation"):
 
 * the teacher is an offline cache of its top-K (id, logit) pairs per token
   (the "Offline distillation" paragraph of that section);

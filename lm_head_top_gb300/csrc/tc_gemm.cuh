@@ -84,7 +84,27 @@ struct GemmShape {
   // group_n): the top-K producer runs one split of every row first, so that
   // the row's other splits start from the threshold it publishes.
   int first_group;
+  // When > 0 (with first_group == 1): split 0 covers n-tiles [0, first_ntiles)
+  // and splits 1.. share the rest evenly; 0: every split gets an even share.
+  int first_ntiles;
 };
+
+// n-tile range [nb, ne) of split s.
+__device__ __forceinline__ void split_range(const GemmShape& sh, int s, int& nb, int& ne) {
+  if (sh.first_ntiles > 0 && sh.nsplit > 1) {
+    if (s == 0) {
+      nb = 0;
+      ne = sh.first_ntiles;
+      return;
+    }
+    const long long rest = sh.n_tiles - sh.first_ntiles;
+    nb = sh.first_ntiles + (int)(((long long)(s - 1) * rest) / (sh.nsplit - 1));
+    ne = sh.first_ntiles + (int)(((long long)s * rest) / (sh.nsplit - 1));
+    return;
+  }
+  nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
+  ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
+}
 
 struct EpiParams {
   // EPI_LSE and EPI_GRAD
@@ -243,8 +263,7 @@ __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, 
     if (u < fg_units) {
       m = u / sh.first_group;
       s = u - m * sh.first_group;
-      nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
-      ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
+      split_range(sh, s, nb, ne);
       return;
     }
     u -= fg_units;
@@ -256,8 +275,7 @@ __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, 
   const int gsize = min(sh.group_n, sh.nsplit - s_base - g * sh.group_n);  // last may be short
   m = r / gsize;
   s = s_base + g * sh.group_n + (r - m * gsize);
-  nb = (int)(((long long)s * sh.n_tiles) / sh.nsplit);
-  ne = (int)(((long long)(s + 1) * sh.n_tiles) / sh.nsplit);
+  split_range(sh, s, nb, ne);
 }
 
 // First position in the sorted id row whose id is >= v (K when none).

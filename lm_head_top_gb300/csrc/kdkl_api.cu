@@ -888,12 +888,15 @@ kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const u
   // One split of every row runs first, alone: the row's other splits then
   // start from the threshold it published instead of compacting from -inf
   // (measured: the MMA's wait on the epilogue halves, 4 % fewer cycles).
-  sh.first_group = f.nsplit > 1 ? 1 : 0;
+  // Only when there are at least as many m-tiles as unit processors: with
+  // fewer, that phase does not fill the GPU and the rows' other splits run
+  // beside it anyway (8K tokens: 6.13 ms without it, 6.19-6.51 with it).
+  sh.first_group = (f.nsplit > 1 && f.m_tiles >= procs) ? 1 : 0;
   // That first split is half as wide as the others' even share: enough
   // vocabulary for a useful threshold, and half as long in the phase where
   // ~all m-tiles are in flight at once and their A rows do not fit in L2.
-  // Measured at 32K tokens against the full-width first split: 26.07 vs
-  // 26.64 ms (5 alternating pairs); a third of the width: 26.39.
+  // Measured at 32K tokens, alternating on one box: 26.04-26.45 ms, against
+  // 26.82-26.86 with no first split and 27.26-27.28 with a full-width one.
   if (sh.first_group) sh.first_ntiles = std::max(1, sh.n_tiles / (2 * sh.nsplit));
   ep.cand = at<float2>(workspace, f.off_cand);
   ep.row_key = at<uint32_t>(workspace, f.off_row_key);

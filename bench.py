@@ -228,11 +228,12 @@ def blas_threads() -> int:
     every core (the OpenBLAS default)."""
     try:
         from threadpoolctl import threadpool_info
+    except ImportError:  # not installed on every host
+        threadpool_info = None
+    if threadpool_info is not None:
         n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
         if n:
             return int(max(n))
-    except Exception:
-        pass
     try:  # the OpenBLAS numpy loaded, asked directly
         import ctypes
         with open("/proc/self/maps") as f:
@@ -247,7 +248,7 @@ def blas_threads() -> int:
                     n = int(fn())
                     if n > 0:
                         return n
-    except Exception:
+    except (OSError, ValueError):  # no /proc, or a library ctypes cannot open
         pass
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         v = os.environ.get(k, "")

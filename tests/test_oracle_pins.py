@@ -332,7 +332,7 @@ def _pins_pass(mod) -> bool:
             return False
         dH, dW = mod.backward(H, W, idx, logit, mask, 2.0)
         return np.allclose(dH, Ht.grad.numpy(), rtol=1e-9) and np.allclose(dW, Wt.grad.numpy(), rtol=1e-9)
-    except Exception:
+    except Exception:  # noqa: BLE001 - a planted mistake that raises fails the pins too
         return False
 
 

@@ -301,7 +301,7 @@ def run_kdkl(args):
         torch.distributed.init_process_group("nccl", device_id=dev)
     kdkl.load()
     w, wname = apply_overrides(WORKLOADS[args.workload], args)
-    x = make_inputs(w, seed=rank, topk_device=dev)
+    x = make_inputs(w, seed=args.seed + rank, topk_device=dev)
     T, d, V, K = w.T, w.d, w.V, w.K
 
     torch.cuda.reset_peak_memory_stats(dev)
@@ -463,7 +463,7 @@ def run_kdkl(args):
                 K, "half from the student's own top-%d" % K if w.teacher == "half_overlap"
                 else "uniform distinct ids"),
             "config": {"workload": wname, "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
-                       "tau": w.tau, "global_batch_tokens": T * world,
+                       "tau": w.tau, "seed": args.seed, "global_batch_tokens": T * world,
                        "parallelism": "dp%d (independent batches)" % world,
                        "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
             "tflops": round(tflops, 1),
@@ -502,7 +502,7 @@ def run_topk(args):
     w = WORKLOADS[args.workload].with_(teacher="uniform")
     if args.tokens:
         w = w.with_(T=args.tokens)
-    x = make_inputs(w, seed=rank)
+    x = make_inputs(w, seed=args.seed + rank)
     T, d, V, K = w.T, w.d, w.V, 100
     torch.cuda.reset_peak_memory_stats(dev)
     H, W = x["H"].to(dev), x["W"].to(dev)
@@ -605,7 +605,7 @@ def run_rkl(args):
         torch.distributed.init_process_group("nccl", device_id=dev)
     kdkl.load()
     w, wname = apply_overrides(WORKLOADS[args.workload], args)
-    x = make_inputs(w, seed=rank, topk_device=dev)
+    x = make_inputs(w, seed=args.seed + rank, topk_device=dev)
     T, d, V, K = w.T, w.d, w.V, w.K
     torch.cuda.reset_peak_memory_stats(dev)
     g = {k: v.to(dev) for k, v in x.items()}
@@ -727,7 +727,7 @@ def run_reference(args):
     if rank != 0:
         return None
     w = WORKLOADS[WORKLOAD]
-    x = make_inputs(w, seed=0)
+    x = make_inputs(w, seed=args.seed)
     x_np = oracle_arrays(x)
     n = args.ref_tokens
     for _ in range(args.warmup):
@@ -766,6 +766,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another workload's shapes, for profiling small cases")
+    ap.add_argument("--seed", type=int, default=0,
+                    help="input seed (rank r of a multi-GPU run uses seed + r)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     ap.add_argument("--K", type=int, default=0, help="override K (config sweeps)")
     ap.add_argument("--tau", type=float, default=0.0, help="override the temperature")

@@ -10,8 +10,10 @@ oracle on its shard, and the reduced results must equal the whole-batch
 oracle. The same host arithmetic drives the CUDA path on N GPUs (no
 collective inside the library).
 
-Also covers bench.py's multi-rank timing rule: the reported time is the max
-over ranks.
+The two loss variants (the mixed soft + hard-label loss and the reverse KL over
+the cached ids) average over the same counted tokens and are checked the same
+way. Also covers bench.py's multi-rank timing rule: the reported time is the
+max over ranks.
 """
 import os
 import socket
@@ -42,6 +44,10 @@ def _problem():
     return H, W, idx, logit, mask, tau
 
 
+def _labels(T, V):
+    return np.random.default_rng(1).integers(0, V, size=T)
+
+
 def _shard(T, rank, world):
     lo = (T * rank) // world
     hi = (T * (rank + 1)) // world
@@ -66,10 +72,28 @@ def _worker(rank, port, out_q):
                                  grad_loss=n_r / N)
         dW = torch.from_numpy(dW_r)
         dist.all_reduce(dW)
+        # the loss variants average over the same counted tokens, so they
+        # shard the same way: the mixed loss, and the reverse KL
+        labels = _labels(H.shape[0], W.shape[0])
+        var = {}
+        for name, fwd, bwd in (
+                ("mixed",
+                 lambda *a: ok.forward_mixed(*a, tau, 0.3, True, labels[lo:hi])[0],
+                 lambda *a, g: ok.backward_mixed(*a, tau, 0.3, True, labels[lo:hi], g)),
+                ("rkl",
+                 lambda *a: ok.reverse_kl_forward(*a, tau)[0],
+                 lambda *a, g: ok.reverse_kl_backward(*a, tau, g))):
+            shard = (H[lo:hi], W, idx[lo:hi], logit[lo:hi], mask[lo:hi])
+            s_r = torch.tensor([fwd(*shard) * n_r], dtype=torch.float64)
+            dist.all_reduce(s_r)
+            vdH, vdW = bwd(*shard, g=n_r / N)
+            vdW = torch.from_numpy(vdW)
+            dist.all_reduce(vdW)
+            var[name] = (s_r.item() / N, vdH, vdW.numpy())
         # bench.py's rule: report the slowest rank's time
         t = torch.tensor([10.0 + rank], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        out_q.put((rank, loss, lo, hi, dH_r, dW.numpy(), t.item()))
+        out_q.put((rank, loss, lo, hi, dH_r, dW.numpy(), t.item(), var))
     finally:
         dist.destroy_process_group()
 
@@ -89,11 +113,23 @@ def test_token_sharded_dp_matches_whole_batch():
     H, W, idx, logit, mask, tau = _problem()
     loss, _, _ = ok.forward(H, W, idx, logit, mask, tau)
     dH, dW = ok.backward(H, W, idx, logit, mask, tau)
-    for rank, loss_g, lo, hi, dH_r, dW_g, tmax in res:
+    labels = _labels(H.shape[0], W.shape[0])
+    whole = {
+        "mixed": (ok.forward_mixed(H, W, idx, logit, mask, tau, 0.3, True, labels)[0],
+                  *ok.backward_mixed(H, W, idx, logit, mask, tau, 0.3, True, labels)),
+        "rkl": (ok.reverse_kl_forward(H, W, idx, logit, mask, tau)[0],
+                *ok.reverse_kl_backward(H, W, idx, logit, mask, tau)),
+    }
+    for rank, loss_g, lo, hi, dH_r, dW_g, tmax, var in res:
         assert abs(loss_g - loss) < 1e-12
         np.testing.assert_allclose(dH_r, dH[lo:hi], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(dW_g, dW, rtol=1e-12, atol=1e-15)
         assert tmax == 10.0 + WORLD - 1
+        for name, (l_w, dH_w, dW_w) in whole.items():
+            l_g, vdH, vdW = var[name]
+            assert abs(l_g - l_w) < 1e-12 * max(1.0, abs(l_w)), name
+            np.testing.assert_allclose(vdH, dH_w[lo:hi], rtol=1e-11, atol=1e-14, err_msg=name)
+            np.testing.assert_allclose(vdW, dW_w, rtol=1e-11, atol=1e-14, err_msg=name)
 
 
 def test_rank_that_never_joins_is_reported():

@@ -34,7 +34,9 @@ METRIC = "fused chunked KL fwd+bwd tokens/s, % of BF16 tensor peak, peak HBM GiB
 WORKLOAD = "gptoss20b_32k"
 SPEC_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_KERNELS = ("fwd_lse_gemm", "bwd_grad_gemm", "dH_gemm", "dW_gemm")
+GEMM_KERNELS = ("fwd_lse_gemm", "bwd_grad_gemm", "dH_gemm", "dW_gemm", "fwd_lse_mix_gemm",
+                "bwd_grad_mix_gemm")
+MIX_ALPHA, MIX_TAU_SQ = 0.5, True  # --path mix: alpha * tau^2 * KL + (1 - alpha) * CE
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -214,6 +216,18 @@ def cpu_baseline(step_fn, x_np, w, n_tokens: int, what: str):
                       % (what, len(rows), w.name, w.V, w.d, t)}
 
 
+def oracle_mix_sample_step(x_np, w, rows, labels, block: int = 1024):
+    """fp64 oracle of the mixed soft + hard-label loss, forward + backward, on
+    a sample of token rows."""
+    import oracle.kl_oracle as ok
+    H, W, idx, logit, mask = x_np
+    for b in range(0, len(rows), block):
+        r = rows[b:b + block]
+        a = (H[r], W, idx[r], logit[r], mask[r], w.tau, MIX_ALPHA, MIX_TAU_SQ, labels[r])
+        ok.forward_mixed(*a)
+        ok.backward_mixed(*a, 1.0)
+
+
 def oracle_arrays(x):
     import oracle.kl_oracle as ok
     return (ok.bf16_bits_to_f64(x["H"].view(torch.int16).numpy()),
@@ -306,10 +320,15 @@ def run_kdkl(args):
 
     torch.cuda.reset_peak_memory_stats(dev)
     g = {k: v.to(dev) for k, v in x.items()}
-    ws_f = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 0), dtype=torch.uint8,
-                       device=dev)
-    ws_b = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 1), dtype=torch.uint8,
-                       device=dev)
+    mix = args.path == "mix"
+    ws_f = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 2 if mix else 0),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 3 if mix else 1),
+                       dtype=torch.uint8, device=dev)
+    # --path mix: hard labels, seeded uniform over the vocabulary
+    labels = torch.randint(0, V, (T,), dtype=torch.int32,
+                           generator=torch.Generator().manual_seed(args.seed + rank)).to(dev)
+    out = {"loss": None}
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     dH = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
@@ -318,6 +337,14 @@ def run_kdkl(args):
 
     def step(gg):
         s = torch.cuda.current_stream(dev)  # the capture stream inside a graph capture
+        if mix:
+            a = (gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"], labels)
+            kw = dict(temperature=w.tau, chunk=w.chunk, alpha=MIX_ALPHA, scale_tau_sq=MIX_TAU_SQ,
+                      stream=s)
+            out["loss"], lse_t, lse_1, _ = kdkl.kd_kl_forward_ex(*a, workspace=ws_f, **kw)
+            kdkl.kd_kl_backward_ex(*a, lse_t, lse_1, grad_loss=1.0, dH=dH, dW=dW, workspace=ws_b,
+                                   **kw)
+            return
         kdkl.kd_kl_forward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"],
                            temperature=w.tau, chunk=w.chunk, loss=loss, lse=lse, workspace=ws_f,
                            stream=s)
@@ -359,7 +386,7 @@ def run_kdkl(args):
     # ---- the same step captured once in a CUDA graph and replayed (launch-bound
     # small shapes); reported beside the eager numbers
     graph_res = None
-    if args.graph:
+    if args.graph and not mix:
         per_step = launches // args.steps
         graph = torch.cuda.CUDAGraph()
         torch.cuda.synchronize(dev)
@@ -403,7 +430,7 @@ def run_kdkl(args):
             for k in gin:
                 gin[k].copy_(host[k], non_blocking=True)
             step(gin)
-            loss_host.copy_(loss, non_blocking=True)
+            loss_host.copy_(out["loss"] if mix else loss, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -436,7 +463,12 @@ def run_kdkl(args):
                     "unit": "GB/s", "frac": None, "traffic": recorded_traffic(dom, run_name)}
         # CPU baseline: the fp64 oracle on a bounded token sample, this host
         cpu = None
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and mix:
+            lab_np = labels.cpu().numpy().astype(np.int64)
+            cpu = cpu_baseline(lambda xn, ww, rows: oracle_mix_sample_step(xn, ww, rows, lab_np),
+                               oracle_arrays(x), w, args.cpu_tokens,
+                               "mixed-loss forward+backward")
+        elif world == 1 and not args.no_cpu_baseline:
             x_np = oracle_arrays(x)
             n_cpu = args.cpu_tokens
             t = time_oracle(x_np, w, n_cpu)[0]
@@ -446,7 +478,8 @@ def run_kdkl(args):
                              "d=%d; dense logits row blocks), %.1f s" % (min(n_cpu, T), wname, V,
                                                                         d, t)}
         result = {
-            "metric": METRIC,
+            "metric": METRIC if not mix else
+            "mixed soft + hard-label distillation loss fwd+bwd tokens/s",
             "value": round(tokens / (elapsed_ms / 1e3), 1),
             "unit": "tokens/s",
             "n_gpus": world,
@@ -481,6 +514,11 @@ def run_kdkl(args):
         }
         if graph_res is not None:
             result["graph"] = graph_res
+        if mix:
+            result["path"] = "mix"
+            result["config"].update({"workload": wname + "_mix", "alpha": MIX_ALPHA,
+                                     "scale_tau_sq": MIX_TAU_SQ,
+                                     "labels": "seeded uniform over the vocabulary"})
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -757,9 +795,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("kdkl", "reference"), default="kdkl")
-    ap.add_argument("--path", choices=("kl", "topk", "rkl"), default="kl",
-                    help="kl: fused KL fwd+bwd (the headline); topk: offline top-K cache "
-                         "producer; rkl: reverse KL over the cached ids")
+    ap.add_argument("--path", choices=("kl", "mix", "topk", "rkl"), default="kl",
+                    help="kl: fused KL fwd+bwd (the headline); mix: the mixed soft + "
+                         "hard-label loss; topk: offline top-K cache producer; rkl: reverse KL "
+                         "over the cached ids")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")

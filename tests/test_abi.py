@@ -162,3 +162,78 @@ def test_rkl_pointer_errors_and_workspace(lib):
     assert abs((sizes[2] - sizes[1]) - (sizes[1] - sizes[0]) * 2) < (1 << 20)
     # T * K must stay below 2^31
     assert kdkl.kd_rkl_workspace_size(1 << 24, 64, 1000, 200) == 0
+
+
+# ---- mixed loss (kd_kl_forward_ex / kd_kl_backward_ex): option checks come
+# back synchronously, before any device call.
+
+def _opts(alpha=0.5, sq=0, labels=64):
+    return kdkl.kd_kl_options(alpha, sq, labels)
+
+
+def _fwd_ex(lib, p, o, lse1=192):
+    P = ctypes.c_void_p
+    return lib.kd_kl_forward_ex(ctypes.byref(p), None if o is None else ctypes.byref(o), P(16),
+                                P(16), P(16), P(16), None, P(64), P(128), P(lse1), None, P(256),
+                                1 << 30, None)
+
+
+def _bwd_ex(lib, p, o, lse1=192):
+    P = ctypes.c_void_p
+    return lib.kd_kl_backward_ex(ctypes.byref(p), None if o is None else ctypes.byref(o), P(16),
+                                 P(16), P(16), P(16), None, P(64), P(lse1), 1.0, P(4096),
+                                 P(8192), 0, P(256), 1 << 30, None)
+
+
+def test_mixed_loss_option_errors_are_synchronous(lib):
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 2.0, 8)
+    for fn in (_fwd_ex, _bwd_ex):
+        assert fn(lib, p, None) == 1                          # no options
+        assert fn(lib, p, _opts(alpha=1.5)) == 1              # alpha outside [0, 1]
+        assert fn(lib, p, _opts(alpha=float("nan"))) == 1
+        assert fn(lib, p, _opts(alpha=0.5, labels=0)) == 1    # CE term without labels
+        assert fn(lib, p, _opts(alpha=0.5, labels=2)) == 3    # labels not 4-byte aligned
+        assert fn(lib, p, _opts(), lse1=0) == 1               # tau != 1 needs lse1
+    bad = kdkl.kd_kl_problem(10, 12, 100, 4, 2.0, 8)          # d % 8 != 0, before the options
+    assert _fwd_ex(lib, bad, _opts(alpha=1.5)) == 3
+    # alpha == 1 needs neither labels nor lse1; the call then reaches the device
+    import torch
+    if not torch.cuda.is_available():
+        assert _fwd_ex(lib, p, _opts(alpha=1.0, labels=0)) in (6, 8)
+    assert lib.kd_kl_workspace_size(ctypes.byref(p), 2) > 0
+    assert lib.kd_kl_workspace_size(ctypes.byref(p), 3) > 0
+
+
+# ---- offline top-K producer (kd_lmhead_topk)
+
+def _topk(lib, p, H=16, W=16, idx=64, val=128, ws=256, ws_bytes=1 << 30):
+    P = ctypes.c_void_p
+    return lib.kd_lmhead_topk(ctypes.byref(p), P(H), P(W), P(idx), P(val), P(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("K", 0, 2), ("K", 257, 2),          # 1..KDKL_TOPK_MAX_K
+    ("K", 101, 2),                       # K > V
+    ("d", 12, 3), ("d", 4, 2), ("T", -1, 2), ("V", 0, 2),
+])
+def test_topk_argument_errors_are_synchronous(lib, field, value, code):
+    p = kdkl.kd_topk_problem(10, 16, 100, 4, 0)
+    setattr(p, field, value)
+    assert _topk(lib, p) == code
+    assert lib.kd_lmhead_topk_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_topk_pointer_errors(lib):
+    p = kdkl.kd_topk_problem(10, 16, 100, 4, 0)
+    assert _topk(lib, p, ws=0) == 5
+    assert _topk(lib, p, H=0) == 1
+    assert _topk(lib, p, W=0) == 1
+    assert _topk(lib, p, idx=0) == 1
+    assert _topk(lib, p, H=8) == 3
+    assert _topk(lib, p, idx=2) == 3
+    import torch
+    if not torch.cuda.is_available():
+        assert _topk(lib, p) in (6, 8)   # a valid call reaches the (absent) device
+    # the workspace grows linearly in T
+    s = [kdkl.kd_lmhead_topk_workspace_size(t, 2880, 201088, 100) for t in (8192, 16384, 32768)]
+    assert s[0] < s[1] < s[2] and abs((s[2] - s[1]) - 2 * (s[1] - s[0])) < (1 << 20)

@@ -61,10 +61,25 @@ int main(void) {
                       (const float*)16, NULL, (float*)64, (float*)128, NULL, NULL, 0,
                       NULL) == KD_ERR_WORKSPACE);
 
+  /* mixed loss: options are checked before anything else happens */
+  CHECK(kd_kl_forward_ex(&p, NULL, (const uint16_t*)16, (const uint16_t*)16, (const int32_t*)16,
+                         (const float*)16, NULL, (float*)64, (float*)128, (float*)192, NULL,
+                         (void*)256, (size_t)1 << 30, NULL) == KD_ERR_INVALID_ARG);
+  kd_kl_options opt = {1.5f, 0, NULL}; /* alpha outside [0, 1] */
+  CHECK(kd_kl_backward_ex(&p, &opt, (const uint16_t*)16, (const uint16_t*)16,
+                          (const int32_t*)16, (const float*)16, NULL, (const float*)64,
+                          (const float*)192, 1.0f, (uint16_t*)4096, (float*)8192, 0, (void*)256,
+                          (size_t)1 << 30, NULL) == KD_ERR_INVALID_ARG);
+  CHECK(kd_kl_workspace_size(&p, 2) > 0 && kd_kl_workspace_size(&p, 3) > 0);
+
   kd_topk_problem tp = {4096, 2880, 201088, 100, 0};
   CHECK(kd_lmhead_topk_workspace_size(&tp) > 0);
+  CHECK(kd_lmhead_topk(&tp, (const uint16_t*)16, (const uint16_t*)16, (int32_t*)64, (float*)128,
+                       NULL, 0, NULL) == KD_ERR_WORKSPACE);
   tp.K = KDKL_TOPK_MAX_K + 1;
   CHECK(kd_lmhead_topk_workspace_size(&tp) == 0);
+  CHECK(kd_lmhead_topk(&tp, (const uint16_t*)16, (const uint16_t*)16, (int32_t*)64, (float*)128,
+                       (void*)256, (size_t)1 << 30, NULL) == KD_ERR_SHAPE);
 
   CHECK(strcmp(kd_status_string(KD_OK), "KD_OK") == 0);
   CHECK(strcmp(kd_status_string(KD_ERR_TIMEOUT), "KD_ERR_TIMEOUT") == 0);

@@ -7,11 +7,12 @@
 //   teacher_prep -> for each block: bwd_grad_gemm -> dH_gemm -> dW_gemm
 //                -> f32_to_bf16 (dH)
 //
-// The pages ("Efficient Knowledge Distillation for LLMs: Offline Top-K Logits
-// and a Fused Chunked KL Loss", page "Making knowledge distillation cheap
-// enough to run at scale", section "Two system changes") process one chunk of
-// sequence positions at a time so memory grows linearly with the sequence and
-// recompute each chunk in backward. Here `chunk` bounds the one buffer that
+// The pages ("Making knowledge distillation cheap enough to run at scale",
+// section "Two system changes"; "Efficient knowledge distillation for LLMs:
+// offline top-K logits and a fused chunked KL loss", section "Two systemic
+// changes for scalable distillation") process one chunk of sequence positions
+// at a time so memory grows linearly with the sequence, and compute each
+// chunk again in backward. Here `chunk` bounds the one buffer that
 // holds gradients of logits (chunk x V bf16). The forward needs no such
 // buffer at all: its epilogue keeps only three floats per token and split.
 // In backward the scheduler tiles the same budget either as `chunk` tokens by

@@ -6,11 +6,9 @@
 //   loss_finalize  one block: ordered sum of the block sums / N.
 //   f32_to_bf16    dH accumulator to bf16 (round to nearest even).
 //
-// Teacher distribution and KL from "Efficient Knowledge Distillation for
-// LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", page "Making
-// knowledge distillation cheap enough to run at scale", section "Two system
-// changes" (top-100 cache per position; the sparse teacher of the
-// forward-chunked and fused variants).
+// Teacher distribution and KL from "Making knowledge distillation cheap
+// enough to run at scale", section "Two system changes" (top-100 cache per
+// position; the sparse teacher of the forward-chunked and fused variants).
 #include <cuda_bf16.h>
 #include <stdint.h>
 

@@ -21,11 +21,12 @@
 // fp32 accumulators in TMEM so the epilogue of one tile overlaps the MMAs of
 // the next.
 //
-// Source of the method: "Efficient Knowledge Distillation for LLMs: Offline
-// Top-K Logits and a Fused Chunked KL Loss", page "Making knowledge
-// distillation cheap enough to run at scale", section "Two system changes"
-// (fused, chunked KL: project a chunk, fold it into the running loss, discard
-// it; recompute in backward).
+// Source of the method: "Making knowledge distillation cheap enough to run at
+// scale", section "Two system changes" (the fused, chunked KL: each chunk's
+// projection is folded into the running loss and discarded, then computed
+// again in backward); the same in "Efficient knowledge distillation for LLMs:
+// offline top-K logits and a fused chunked KL loss", section "Two systemic
+// changes for scalable distillation".
 #pragma once
 
 #include <cuda_bf16.h>

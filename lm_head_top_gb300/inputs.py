@@ -5,12 +5,13 @@ library consumes. It holds none of the loss's arithmetic: no softmax, no
 logsumexp, no KL, no gradient. Both the CUDA path and the CPU oracle are fed
 the tensors it returns, so a parity test compares the two on identical bytes.
 
-Workloads stand in for the pages' own runs ("Efficient Knowledge Distillation
-for LLMs: Offline Top-K Logits and a Fused Chunked KL Loss"): the 8K-context
-Llama-3.2-3B-like student (that page's "Performance and memory benchmarks"
-table), the GPT-OSS-20B run at 32,768 tokens ("Scaling to long contexts"),
-and the toy output-projection
-benchmark that runs to 256K tokens. The real models, teacher caches and
+Workloads stand in for the pages' own runs: the 8K-context Llama-3.2-3B-like
+student ("Efficient knowledge distillation for LLMs: offline top-K logits and
+a fused chunked KL loss", table of section "Performance and memory
+benchmarks"), the GPT-OSS-20B run at 32,768 tokens and the toy
+output-projection benchmark that runs to 256K tokens ("Making knowledge
+distillation cheap enough to run at scale", section "Scaling to long
+contexts"). The real models, teacher caches and
 training data are not used: every tensor is synthetic.
 
 Recipe (all from ``numpy.random.SeedSequence(seed)``, one child stream per

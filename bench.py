@@ -203,6 +203,21 @@ def step_stats(ev0, marks):
     return round(float(np.median(ms)), 3), round(float(min(ms)), 3)
 
 
+def kernel_pass(kdkl, step_fn, steps: int, stream, dev):
+    """Runs `steps` more steps with the library's per-launch event timing on;
+    returns [(kernel, launches, total ms)] and the pass's own elapsed ms."""
+    torch.cuda.synchronize(dev)
+    kdkl.kd_timing_begin()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step_fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    rows = kdkl.kd_timing_end()
+    return rows, a.elapsed_time(b)
+
+
 def cpu_baseline(step_fn, x_np, w, n_tokens: int, what: str):
     """Times step_fn (an oracle sample step) on n_tokens random rows of w."""
     rng = np.random.default_rng(0)
@@ -323,7 +338,8 @@ def run_kdkl(args):
     mix = args.path == "mix"
     ws_f = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 2 if mix else 0),
                        dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 3 if mix else 1),
+    # the backward reuses the teacher rows the forward prepared in ws_f
+    ws_b = torch.empty(kdkl.kd_kl_workspace_size(T, d, V, K, w.tau, w.chunk, 4),
                        dtype=torch.uint8, device=dev)
     # --path mix: hard labels, seeded uniform over the vocabulary
     labels = torch.randint(0, V, (T,), dtype=torch.int32,
@@ -343,14 +359,14 @@ def run_kdkl(args):
                       stream=s)
             out["loss"], lse_t, lse_1, _ = kdkl.kd_kl_forward_ex(*a, workspace=ws_f, **kw)
             kdkl.kd_kl_backward_ex(*a, lse_t, lse_1, grad_loss=1.0, dH=dH, dW=dW, workspace=ws_b,
-                                   **kw)
+                                   fwd_workspace=ws_f, **kw)
             return
         kdkl.kd_kl_forward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"],
                            temperature=w.tau, chunk=w.chunk, loss=loss, lse=lse, workspace=ws_f,
                            stream=s)
         kdkl.kd_kl_backward(gg["H"], g["W"], gg["topk_idx"], gg["topk_logit"], gg["mask"], lse,
                             temperature=w.tau, chunk=w.chunk, grad_loss=1.0, dH=dH, dW=dW,
-                            workspace=ws_b, stream=s)
+                            workspace=ws_b, fwd_workspace=ws_f, stream=s)
 
     for _ in range(args.warmup):
         step(g)
@@ -361,13 +377,13 @@ def run_kdkl(args):
         raise SystemExit("device status after warm-up: %s / %s" % (kdkl.kd_status_string(st),
                                                                    kdkl.kd_status_string(st_b)))
 
-    # ---- device-resident timed region
+    # ---- device-resident timed region: the steps alone, bracketed by two
+    # events (and one event per step for the spread); no per-kernel timing
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kdkl.kd_launch_count()
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        kdkl.kd_timing_begin()
         marks = step_marks(args.steps)
         ev0.record(stream)
         for i in range(args.steps):
@@ -375,13 +391,17 @@ def run_kdkl(args):
             marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        per_kernel = kdkl.kd_timing_end()
         barrier(world)
     launches = kdkl.kd_launch_count() - launches0
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     clk = clocks.summary()
     peak_hbm = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+
+    # ---- per-kernel device times: the same steps again, every launch
+    # bracketed by events on its stream (a separate pass, so the events do not
+    # sit inside the headline timing)
+    per_kernel, prof_ms = kernel_pass(kdkl, lambda: step(g), args.steps, stream, dev)
 
     # ---- the same step captured once in a CUDA graph and replayed (launch-bound
     # small shapes); reported beside the eager numbers
@@ -507,9 +527,13 @@ def run_kdkl(args):
             "cpu_baseline": cpu,
             "e2e": None if e2e_ms is None else {
                 "value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                "copies": "in: H, topk_idx, topk_logit, mask from pinned host memory; out: the "
+                          "loss (4 bytes). dH and dW stay on the device, where a training "
+                          "step's optimizer consumes them"},
             "gpu_launches": launches,
             "kernel_ms_per_step": {n: round(ms / args.steps, 3) for n, c, ms in per_kernel},
+            "kernel_pass_ms_per_step": round(prof_ms / args.steps, 3),
             "clocks": clk,
         }
         if graph_res is not None:
@@ -560,7 +584,6 @@ def run_topk(args):
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        kdkl.kd_timing_begin()
         marks = step_marks(args.steps)
         ev0.record(stream)
         for i in range(args.steps):
@@ -568,11 +591,11 @@ def run_topk(args):
             marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     launches = kdkl.kd_launch_count() - launches0
+    per_kernel, _ = kernel_pass(kdkl, step, args.steps, stream, dev)
 
     # ---- end to end: pinned host H copied in, the cache (ids + logits) read back
     e2e = None
@@ -672,7 +695,6 @@ def run_rkl(args):
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        kdkl.kd_timing_begin()
         marks = step_marks(args.steps)
         ev0.record(stream)
         for i in range(args.steps):
@@ -680,11 +702,11 @@ def run_rkl(args):
             marks[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        per_kernel = kdkl.kd_timing_end()
         barrier(world)
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     med_ms, min_ms = step_stats(ev0, marks)  # this rank's steps
     launches = kdkl.kd_launch_count() - launches0
+    per_kernel, _ = kernel_pass(kdkl, step, args.steps, stream, dev)
 
     # ---- end to end: pinned host H and teacher cache copied in, loss read back
     e2e = None

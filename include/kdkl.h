@@ -72,7 +72,8 @@ typedef struct {
 } kd_kl_problem;
 
 /* Workspace bytes for kd_kl_forward (which = 0), kd_kl_backward (which = 1),
- * kd_kl_forward_ex (which = 2) or kd_kl_backward_ex (which = 3).
+ * kd_kl_forward_ex (which = 2), kd_kl_backward_ex (which = 3) or
+ * kd_kl_backward_reuse (which = 4).
  * Linear in T (no T x V term). Returns 0 if the problem is invalid. */
 size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which);
 
@@ -141,6 +142,32 @@ kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts
                             int accumulate_dW, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Backward that reuses the teacher cache the forward already prepared. The
+ * forward turns the cache into sorted (id, p) rows and counts the mask
+ * (N) in its workspace; the pages compute the teacher side once and keep it
+ * ("Making knowledge distillation cheap enough to run at scale", section "Two
+ * system changes"), so the backward can read those rows instead of preparing
+ * them again. Same results as kd_kl_backward / kd_kl_backward_ex.
+ *   opts           NULL for the plain KL loss, else as kd_kl_backward_ex
+ *   mask, lse, lse1  as kd_kl_backward(_ex); mask must be the forward's
+ *   fwd_workspace  the workspace of the latest kd_kl_forward or
+ *                  kd_kl_forward_ex call on the same problem (T, d, V, K and
+ *                  temperature; chunk may differ), queued earlier on the same
+ *                  stream and not reused since; read only
+ *   workspace      kd_kl_workspace_size(prob, 4) bytes (no teacher region)
+ * The library remembers, on the host, which problem each forward workspace
+ * was last filled for; a fwd_workspace it does not know for this problem, or
+ * fwd_workspace_bytes smaller than that call's, returns KD_ERR_INVALID_ARG
+ * synchronously. The teacher cache was validated by the forward: its
+ * device-detected errors are read from fwd_workspace, this call's (wait
+ * timeouts) from workspace. */
+kd_status kd_kl_backward_reuse(const kd_kl_problem* prob, const kd_kl_options* opts,
+                               const uint16_t* H, const uint16_t* W, const uint8_t* mask,
+                               const float* lse, const float* lse1, const void* fwd_workspace,
+                               size_t fwd_workspace_bytes, float grad_loss, uint16_t* dH,
+                               float* dW, int accumulate_dW, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* Allocation-free forward. The paper has no counterpart to this call; it
  * exists for callers that cannot allocate device memory for a workspace: code
  * inside a host framework whose memory pool owns (and has typically reserved)
@@ -152,20 +179,27 @@ kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts
  * the process exits. Problems whose kd_kl_workspace_size(prob, 0) exceeds it
  * return KD_ERR_WORKSPACE before anything is queued.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current), and so does the first
+ *     call after a device reset; make that first call before any stream
+ *     capture.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine (with
  *     per-kernel timing off, the default).
  *   - Every call on a device shares the one array and clears its header when
  *     it starts. Calls whose GPU work overlaps (other streams, other host
  *     threads) race on it: order them on one stream.
- *   - Device-detected errors of these calls cannot be read back with
- *     kd_kl_check_status (there is no workspace pointer to pass). */
+ *   - Device-detected errors (an id outside [0, V), a teacher row with no
+ *     finite logit, a wait that ran out) go to the array's status word and are
+ *     read with kd_kl_noalloc_check_status(); outputs are then undefined. */
 #define KDKL_NOALLOC_SCRATCH_BYTES (64u << 20)
 kd_status kd_kl_forward_noalloc(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                                 const int32_t* topk_idx, const float* topk_logit,
                                 const uint8_t* mask, float* loss, float* lse, float* token_kl,
                                 void* stream);
+
+/* BLOCKING: synchronises `stream`, then returns the first device-detected
+ * error recorded by the latest kd_kl_forward_noalloc call on the current
+ * device (KD_OK if none), like kd_kl_check_status does for a workspace. */
+kd_status kd_kl_noalloc_check_status(void* stream);
 
 /* ---------------------------------------------------------------------------
  * Second loss variant: reverse KL restricted to the cached ids. The pages

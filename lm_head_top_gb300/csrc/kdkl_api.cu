@@ -240,7 +240,9 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, 
   return f;
 }
 
-BwdPlan plan_backward(const kd_kl_problem& p) {
+// own_teacher: the backward prepares the sorted teacher cache itself (sidx,
+// sp in its workspace); otherwise it reads the forward's.
+BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
   BwdPlan b{};
   const int64_t T = std::max<int64_t>(p.T, 1);
   const double budget = (double)p.chunk * (double)p.V;  // gradient-of-logits elements
@@ -263,7 +265,7 @@ BwdPlan plan_backward(const kd_kl_problem& p) {
   b.Tb_pad = round_up(b.Tb, BM);
   b.Vb_pad = round_up(b.Vb, LOGIT_BN);
   size_t o = kHeaderBytes;
-  const size_t TK = (size_t)p.T * p.K;
+  const size_t TK = own_teacher ? (size_t)p.T * p.K : 0;
   b.off_sidx = o; o = align256(o + TK * 4);
   b.off_sp = o; o = align256(o + TK * 4);
   b.off_G = o; o = align256(o + (size_t)b.Tb_pad * b.Vb_pad * 2);
@@ -396,6 +398,52 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// Forward workspaces whose prepared teacher cache a backward may reuse: the
+// problem each one was last filled for by a forward call that queued all its
+// work. A forward call drops its workspace's entry when it starts and adds it
+// back when it has queued everything, so a failed call leaves none.
+struct FwdRecord {
+  const void* ws;
+  int64_t T, d, V;
+  int32_t K;
+  float temperature;
+  size_t bytes;
+};
+constexpr size_t kMaxFwdRecords = 64;
+std::mutex g_fwd_mu;
+std::vector<FwdRecord> g_fwd_records;
+
+void forget_forward(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_fwd_mu);
+  for (size_t i = 0; i < g_fwd_records.size(); ++i)
+    if (g_fwd_records[i].ws == ws) {
+      g_fwd_records.erase(g_fwd_records.begin() + (long)i);
+      return;
+    }
+}
+
+void remember_forward(const void* ws, const kd_kl_problem& p, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_fwd_mu);
+  for (size_t i = 0; i < g_fwd_records.size(); ++i)
+    if (g_fwd_records[i].ws == ws) {
+      g_fwd_records.erase(g_fwd_records.begin() + (long)i);
+      break;
+    }
+  if (g_fwd_records.size() >= kMaxFwdRecords) g_fwd_records.erase(g_fwd_records.begin());
+  g_fwd_records.push_back(FwdRecord{ws, p.T, p.d, p.V, p.K, p.temperature, bytes});
+}
+
+// True when `ws` was last filled by a forward call on the same problem (chunk
+// aside: it does not change the teacher cache) and is at least `bytes` long.
+bool forward_matches(const void* ws, size_t ws_bytes, const kd_kl_problem& p) {
+  std::lock_guard<std::mutex> lk(g_fwd_mu);
+  for (const FwdRecord& r : g_fwd_records)
+    if (r.ws == ws)
+      return r.T == p.T && r.d == p.d && r.V == p.V && r.K == p.K &&
+             r.temperature == p.temperature && ws_bytes >= r.bytes;
+  return false;
+}
+
 #define KD_CUDA(x)                              \
   do {                                          \
     if ((x) != cudaSuccess) return KD_ERR_CUDA; \
@@ -442,6 +490,7 @@ size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which) {
     return total;
   }
   if (which == 1 || which == 3) return plan_backward(*prob).total;
+  if (which == 4) return plan_backward(*prob, false).total;
   return 0;
 }
 
@@ -500,12 +549,14 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
   const FwdPlan f = plan_forward(p, di.num_sms, pair, gemm_procs(di.num_sms, pair), mix);
   if (workspace_bytes < f.total) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  forget_forward(workspace);
 
   int* status = at<int>(workspace, 0);
   int* n_count = status + 1;
   KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
   if (p.T == 0) {
     KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
+    remember_forward(workspace, p, f.off_sp);
     return KD_OK;
   }
   const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
@@ -563,6 +614,8 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
                                token_kl, bsum, stream));
   }
   KD_CUDA(launch_loss_finalize(bsum, combine_blocks(T), n_count, loss, stream));
+  // the teacher region (header, sorted ids, their p) is what a backward reuses
+  remember_forward(workspace, p, f.off_sp + (size_t)p.T * p.K * 4);
   return KD_OK;
 }
 
@@ -589,9 +642,15 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
                                const float* topk_logit, const uint8_t* mask, const float* lse,
                                const float* lse1, float grad_loss, uint16_t* dH, float* dW,
                                int accumulate_dW, void* workspace, size_t workspace_bytes,
-                               void* stream_ptr) {
-  kd_status st = validate_common(prob, H, W, topk_idx, topk_logit, workspace);
+                               void* stream_ptr, const void* fwd_ws = nullptr,
+                               size_t fwd_ws_bytes = 0) {
+  const bool reuse = fwd_ws != nullptr;
+  // With a reused forward workspace the teacher cache is not read: stand-in
+  // non-null pointers pass the common checks.
+  kd_status st = validate_common(prob, H, W, reuse ? fwd_ws : topk_idx,
+                                 reuse ? fwd_ws : topk_logit, workspace);
   if (st != KD_OK) return st;
+  if (reuse && !forward_matches(fwd_ws, fwd_ws_bytes, *prob)) return KD_ERR_INVALID_ARG;
   const bool mix = opts != nullptr;
   if (mix && ((st = validate_options(prob, opts)) != KD_OK)) return st;
   // temperature-1 logsumexp: needed when the CE term is on and tau != 1
@@ -605,12 +664,13 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   if ((st = device_info(&di)) != KD_OK) return st;
   if ((st = get_encoder()) != KD_OK) return st;
   const kd_kl_problem& p = *prob;
-  const BwdPlan b = plan_backward(p);
+  const BwdPlan b = plan_backward(p, !reuse);
   if (workspace_bytes < b.total) return KD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   int* status = at<int>(workspace, 0);
-  int* n_count = status + 1;
+  // the counted-token total N: this call's own, or the forward's
+  int* n_count = reuse ? const_cast<int*>(static_cast<const int*>(fwd_ws)) + 1 : status + 1;
   KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
   if (p.T == 0) {
     if (!accumulate_dW) KD_CUDA(cudaMemsetAsync(dW, 0, (size_t)p.V * p.d * 4, stream));
@@ -619,13 +679,17 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
   const float inv_tau = 1.0f / p.temperature;
   const float cl2 = 1.4426950408889634f * inv_tau;
-  int32_t* sidx = at<int32_t>(workspace, b.off_sidx);
-  float* sp = at<float>(workspace, b.off_sp);
+  // Sorted teacher ids and probabilities: the forward workspace's (same
+  // offsets in both layouts), or prepared here.
+  void* tws = reuse ? const_cast<void*>(fwd_ws) : workspace;
+  int32_t* sidx = at<int32_t>(tws, b.off_sidx);
+  float* sp = at<float>(tws, b.off_sidx + align256((size_t)p.T * p.K * 4));
   uint16_t* Gbuf = at<uint16_t>(workspace, b.off_G);
   float* dH_acc = at<float>(workspace, b.off_dH);
 
-  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
-                              inv_tau, sidx, sp, nullptr, n_count, status, stream));
+  if (!reuse)
+    KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
+                                inv_tau, sidx, sp, nullptr, n_count, status, stream));
 
   const bool pair = use_pair();
   const int tile_m = pair ? 2 * BM : BM;
@@ -763,6 +827,18 @@ kd_status kd_kl_backward_ex(const kd_kl_problem* prob, const kd_kl_options* opts
   if (!opts) return KD_ERR_INVALID_ARG;
   return backward_impl(prob, opts, H, W, topk_idx, topk_logit, mask, lse, lse1, grad_loss, dH, dW,
                        accumulate_dW, workspace, workspace_bytes, stream);
+}
+
+kd_status kd_kl_backward_reuse(const kd_kl_problem* prob, const kd_kl_options* opts,
+                               const uint16_t* H, const uint16_t* W, const uint8_t* mask,
+                               const float* lse, const float* lse1, const void* fwd_workspace,
+                               size_t fwd_workspace_bytes, float grad_loss, uint16_t* dH,
+                               float* dW, int accumulate_dW, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!fwd_workspace) return KD_ERR_INVALID_ARG;
+  return backward_impl(prob, opts, H, W, nullptr, nullptr, mask, lse, lse1, grad_loss, dH, dW,
+                       accumulate_dW, workspace, workspace_bytes, stream, fwd_workspace,
+                       fwd_workspace_bytes);
 }
 
 static bool rkl_problem_ok(const kd_kl_problem* p) {

@@ -11,105 +11,237 @@
 // position; the sparse teacher of the forward-chunked and fused variants).
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "kdkl_internal.h"
 #include "tc_primitives.cuh"
 
 namespace kdkl {
 
-constexpr int PREP_WARPS = 8;
+// teacher_prep: a row of K cached entries is handled by L lanes (16 or 32) of
+// a warp, lane l holding elements l*E .. l*E+E-1 of the row padded to
+// N = L*E (a power of two >= K). The row is read from global memory once, into
+// registers; the teacher softmax, its entropy term and the validation run
+// there. The (id, p) pairs are then ordered by id with a bitonic network on
+// packed keys (id, original position): the first log2(E) levels of every
+// merge stay inside a lane, the rest exchange keys with __shfl_xor_sync, and
+// p follows through a per-row shared-memory slot indexed by the original
+// position. Packed keys are distinct, so the network needs no tie rule.
+constexpr int PREP_THREADS = 256;
 
-// One warp per token row. Dynamic shared memory: PREP_WARPS * p2 * 8 bytes.
-__global__ void __launch_bounds__(PREP_WARPS * 32)
+template <int N>
+struct Log2 {
+  static constexpr int value = 1 + Log2<N / 2>::value;
+};
+template <>
+struct Log2<1> {
+  static constexpr int value = 0;
+};
+
+template <bool WIDE>
+struct PrepKey;
+template <>
+struct PrepKey<false> {  // id << log2(N) | position: V * N <= 2^32
+  using T = uint32_t;
+  static constexpr T pad = 0xffffffffu;
+};
+template <>
+struct PrepKey<true> {  // id << 32 | position
+  using T = unsigned long long;
+  static constexpr T pad = ~0ull;
+};
+
+__device__ __forceinline__ uint32_t shfl_key(uint32_t v, int o) {
+  return __shfl_xor_sync(0xffffffffu, v, o);
+}
+__device__ __forceinline__ unsigned long long shfl_key(unsigned long long v, int o) {
+  return __shfl_xor_sync(0xffffffffu, v, o);
+}
+
+// Sum / max over the L lanes of one row (xor offsets below L stay in the row).
+template <int L>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = L / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int L>
+__device__ __forceinline__ float row_max(float v) {
+#pragma unroll
+  for (int o = L / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int L, int E, bool WIDE>
+__global__ void __launch_bounds__(PREP_THREADS)
     teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logit,
                         const uint8_t* __restrict__ mask, const int32_t* __restrict__ labels,
-                        int T, int K, int p2, int V, float inv_tau, int32_t* __restrict__ sidx,
+                        int T, int K, int V, float inv_tau, int vec_io, int32_t* __restrict__ sidx,
                         float* __restrict__ sp, float* __restrict__ ent, int* n_count,
                         int* status) {
-  extern __shared__ uint8_t prep_smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* keys = reinterpret_cast<int*>(prep_smem) + warp * p2;
-  float* vals = reinterpret_cast<float*>(prep_smem + (size_t)PREP_WARPS * p2 * 4) + warp * p2;
-  const int t = blockIdx.x * PREP_WARPS + warp;
+  using Key = typename PrepKey<WIDE>::T;
+  constexpr int N = L * E;
+  constexpr int LOGN = Log2<N>::value;
+  constexpr int ROWS = PREP_THREADS / L;  // rows per block
+  __shared__ float p_slot[ROWS * N];
   __shared__ int block_count;
+  const int lane = threadIdx.x & 31;
+  const int row = threadIdx.x / L;  // row slot in the block
+  const int l = threadIdx.x % L;    // lane within the row
+  const int t = blockIdx.x * ROWS + row;
+  const bool live = t < T;
   if (threadIdx.x == 0) block_count = 0;
   __syncthreads();
 
-  if (t < T) {
-    const int32_t* irow = idx + (long long)t * K;
-    const float* lrow = logit + (long long)t * K;
-    // max of a = logit / tau; validate ids and logits
-    float amax = -INFINITY;
-    bool bad_id = false, bad_logit = false;
-    for (int k = lane; k < K; k += 32) {
-      const int id = __ldg(irow + k);
-      const float a = __ldg(lrow + k) * inv_tau;
-      bad_id |= (id < 0 || id >= V);
-      bad_logit |= (a != a) || (a == INFINITY);
-      amax = fmaxf(amax, a);
-    }
+  // ---- one read of the row into registers
+  int id[E];
+  float a[E];
+  const long long base = (long long)(live ? t : 0) * K;
+  // 16-byte loads and stores when rows and pointers allow (host-checked)
+  const bool vec4 = (E % 4 == 0) && vec_io != 0;
+  if (vec4) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (__any_sync(0xffffffffu, bad_id) && lane == 0) record_error(status, DEV_ERR_INDEX_RANGE);
-    const bool no_finite = !(amax > -INFINITY);
-    if ((__any_sync(0xffffffffu, bad_logit) || no_finite) && lane == 0)
-      record_error(status, DEV_ERR_INVALID_ARG);
-    // sum of exp(a - max)
-    float sum = 0.f;
-    for (int k = lane; k < K; k += 32) sum += expf(__ldg(lrow + k) * inv_tau - amax);
+    for (int j = 0; j < E; j += 4) {
+      const int k = l * E + j;
+      const bool in = live && k < K;  // all four in or all out (K % 4 == 0)
+      const int4 iv = in ? __ldg(reinterpret_cast<const int4*>(idx + base + k)) : make_int4(0, 0, 0, 0);
+      const float4 lv = in ? __ldg(reinterpret_cast<const float4*>(logit + base + k))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      id[j] = iv.x, id[j + 1] = iv.y, id[j + 2] = iv.z, id[j + 3] = iv.w;
+      a[j] = lv.x * inv_tau, a[j + 1] = lv.y * inv_tau, a[j + 2] = lv.z * inv_tau,
+      a[j + 3] = lv.w * inv_tau;
+    }
+  } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float log_sum = logf(sum);
-    // p, entropy term sum p log p, and the (id, p) pairs to sort
-    float h = 0.f;
-    for (int k = lane; k < p2; k += 32) {
-      if (k < K) {
-        const float a = __ldg(lrow + k) * inv_tau - amax;  // <= 0 or -inf
-        const float p = no_finite ? 0.f : expf(a) / sum;
-        if (p > 0.f) h += p * (a - log_sum);
-        keys[k] = __ldg(irow + k);
-        vals[k] = p;
-      } else {
-        keys[k] = 0x7fffffff;
-        vals[k] = 0.f;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
-    __syncwarp();
-    // bitonic sort of p2 (power of two) pairs, ascending by id
-    for (int size = 2; size <= p2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = lane; i < (p2 >> 1); i += 32) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool ascending = (lo & size) == 0;
-          const int klo = keys[lo], khi = keys[hi];
-          if ((klo > khi) == ascending) {
-            keys[lo] = khi;
-            keys[hi] = klo;
-            const float vlo = vals[lo];
-            vals[lo] = vals[hi];
-            vals[hi] = vlo;
-          }
-        }
-        __syncwarp();
-      }
-    }
-    int32_t* so = sidx + (long long)t * K;
-    float* po = sp + (long long)t * K;
-    for (int k = lane; k < K; k += 32) {
-      so[k] = keys[k];
-      po[k] = vals[k];
-    }
-    if (lane == 0) {
-      if (labels && (labels[t] < 0 || labels[t] >= V)) record_error(status, DEV_ERR_INDEX_RANGE);
-      if (ent) ent[t] = h;
-      if (mask == nullptr || mask[t] != 0) atomicAdd(&block_count, 1);
+    for (int j = 0; j < E; ++j) {
+      const int k = l * E + j;
+      const bool in = live && k < K;
+      id[j] = in ? __ldg(idx + base + k) : 0;
+      a[j] = in ? __ldg(logit + base + k) * inv_tau : -INFINITY;
     }
   }
+
+  // ---- validation, max of a = logit / tau
+  bool bad_id = false, bad_logit = false;
+  float amax = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const bool in = live && l * E + j < K;
+    bad_id |= in && (id[j] < 0 || id[j] >= V);
+    bad_logit |= in && ((a[j] != a[j]) || (a[j] == INFINITY));
+    amax = fmaxf(amax, a[j]);
+  }
+  amax = row_max<L>(amax);
+  const bool no_finite = !(amax > -INFINITY);
+  {
+    // one report per warp is enough: the status keeps the first error
+    const bool idx_err = __any_sync(0xffffffffu, bad_id);
+    const bool arg_err = __any_sync(0xffffffffu, bad_logit || (live && no_finite));
+    if (lane == 0 && idx_err) record_error(status, DEV_ERR_INDEX_RANGE);
+    if (lane == 0 && arg_err) record_error(status, DEV_ERR_INVALID_ARG);
+  }
+
+  // ---- teacher softmax over the K entries and sum p log p (0 log 0 = 0)
+  float e[E];
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    e[j] = no_finite ? 0.f : expf(a[j] - amax);  // exp(-inf) = 0 for -inf and padding
+    sum += e[j];
+  }
+  sum = row_sum<L>(sum);
+  const float log_sum = logf(sum);
+  float h = 0.f;
+  float* ps = p_slot + row * N;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const float p = no_finite ? 0.f : e[j] / sum;
+    if (p > 0.f) h += p * ((a[j] - amax) - log_sum);
+    ps[l * E + j] = p;
+  }
+  h = row_sum<L>(h);
+
+  // ---- order the entries by id: bitonic network over packed keys
+  Key key[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int k = l * E + j;
+    const bool in = live && k < K;
+    key[j] = !in ? PrepKey<WIDE>::pad
+                 : (WIDE ? (((Key)(uint32_t)id[j]) << 32) | (Key)k
+                         : (((Key)(uint32_t)id[j]) << LOGN) | (Key)k);
+  }
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= E) {  // partner in lane l ^ (stride / E), same slot
+        const int lo_side = ((l * E) & stride) == 0;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          const bool asc = (((l * E + j) & size) == 0);
+          const Key o = shfl_key(key[j], stride / E);
+          const bool keep_min = (lo_side != 0) == asc;
+          key[j] = keep_min ? (o < key[j] ? o : key[j]) : (o > key[j] ? o : key[j]);
+        }
+      } else {  // partner in this lane, slot j ^ stride
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if ((j & stride) == 0) {
+            const bool asc = (((l * E + j) & size) == 0);
+            const Key x = key[j], y = key[j + stride];
+            const bool swap = asc ? (x > y) : (x < y);
+            key[j] = swap ? y : x;
+            key[j + stride] = swap ? x : y;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---- write the sorted (id, p) row
+  if (live) {
+    int32_t* so = sidx + base;
+    float* po = sp + base;
+    int oid[E];
+    float op[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int pos = (int)(key[j] & (Key)(WIDE ? 0xffffffffu : (uint32_t)(N - 1)));
+      oid[j] = (int32_t)(uint32_t)(WIDE ? (key[j] >> 32) : (key[j] >> LOGN));
+      op[j] = ps[pos & (N - 1)];
+    }
+    if (vec4) {
+#pragma unroll
+      for (int j = 0; j < E; j += 4) {
+        const int k = l * E + j;
+        if (k < K) {
+          *reinterpret_cast<int4*>(so + k) = make_int4(oid[j], oid[j + 1], oid[j + 2], oid[j + 3]);
+          *reinterpret_cast<float4*>(po + k) = make_float4(op[j], op[j + 1], op[j + 2], op[j + 3]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const int k = l * E + j;
+        if (k < K) {
+          so[k] = oid[j];
+          po[k] = op[j];
+        }
+      }
+    }
+    if (l == 0) {
+      if (labels && (labels[t] < 0 || labels[t] >= V)) record_error(status, DEV_ERR_INDEX_RANGE);
+      if (ent) ent[t] = h;
+    }
+  }
+  const bool counted = live && l == 0 && (mask == nullptr || mask[t] != 0);
+  const uint32_t cnt = __popc(__ballot_sync(0xffffffffu, counted));
+  if (lane == 0 && cnt) atomicAdd(&block_count, (int)cnt);
   __syncthreads();
   if (threadIdx.x == 0 && block_count) atomicAdd(n_count, block_count);
 }
@@ -364,18 +496,50 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------ host launchers
 
+namespace {
+
+template <int L, int E>
+cudaError_t launch_prep(bool wide, const int32_t* idx, const float* logit, const uint8_t* mask,
+                        const int32_t* labels, int T, int K, int V, float inv_tau, int vec_io,
+                        int32_t* sidx,
+                        float* sp, float* ent, int* n_count, int* status, cudaStream_t stream) {
+  constexpr int rows = PREP_THREADS / L;
+  const dim3 grid((T + rows - 1) / rows);
+  if (wide)
+    return launch_kernel("teacher_prep", teacher_prep_kernel<L, E, true>, grid, dim3(PREP_THREADS),
+                         0, stream, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp,
+                         ent, n_count, status);
+  return launch_kernel("teacher_prep", teacher_prep_kernel<L, E, false>, grid, dim3(PREP_THREADS),
+                       0, stream, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp,
+                       ent, n_count, status);
+}
+
+}  // namespace
+
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
                                 const int32_t* labels, int T, int K, int V, float inv_tau,
                                 int32_t* sidx, float* sp, float* ent, int* n_count, int* status,
                                 cudaStream_t stream) {
-  int p2 = 1;
-  while (p2 < K) p2 <<= 1;
-  if (p2 < 2) p2 = 2;
-  const size_t smem = (size_t)PREP_WARPS * p2 * 8;
-  const int blocks = (T + PREP_WARPS - 1) / PREP_WARPS;
-  return launch_kernel("teacher_prep", teacher_prep_kernel, dim3(blocks), dim3(PREP_WARPS * 32),
-                       smem, stream, idx, logit, mask, labels, T, K, p2, V, inv_tau, sidx, sp,
-                       ent, n_count, status);
+  // Rows of up to 128 entries take 16 lanes (two rows per warp), longer rows
+  // a whole warp. Packed 32-bit keys when every id fits beside the position.
+  int n = 16;
+  while (n < K) n <<= 1;
+  // KDKL_PREP_WIDE=1 (test hook, read per call) takes the 64-bit keys anyway.
+  const char* force_wide = getenv("KDKL_PREP_WIDE");
+  const bool wide = (unsigned long long)V * (unsigned long long)n >= (1ull << 32) ||
+                    (force_wide && force_wide[0] == '1');
+  auto a16 = [](const void* q) { return ((uintptr_t)q & 15u) == 0; };
+  const int vec_io = (K % 4 == 0 && a16(idx) && a16(logit) && a16(sidx) && a16(sp)) ? 1 : 0;
+#define KDKL_PREP(L, E)                                                                     \
+  launch_prep<L, E>(wide, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp, ent,  \
+                    n_count, status, stream)
+  if (K <= 16) return KDKL_PREP(16, 1);
+  if (K <= 32) return KDKL_PREP(16, 2);
+  if (K <= 64) return KDKL_PREP(16, 4);
+  if (K <= 128) return KDKL_PREP(16, 8);
+  if (K <= 256) return KDKL_PREP(32, 8);
+  return KDKL_PREP(32, 16);
+#undef KDKL_PREP
 }
 
 int combine_blocks(int T) { return (T + COMBINE_THREADS - 1) / COMBINE_THREADS; }

@@ -81,6 +81,17 @@ int main(void) {
   CHECK(kd_lmhead_topk(&tp, (const uint16_t*)16, (const uint16_t*)16, (int32_t*)64, (float*)128,
                        (void*)256, (size_t)1 << 30, NULL) == KD_ERR_SHAPE);
 
+  /* the backward that reuses a forward's teacher rows: smaller workspace, and
+   * a forward workspace the library has not seen filled is refused on the host */
+  CHECK(kd_kl_workspace_size(&p, 4) > 0 && kd_kl_workspace_size(&p, 4) < bwd);
+  CHECK(kd_kl_backward_reuse(&p, NULL, (const uint16_t*)16, (const uint16_t*)16, NULL,
+                             (const float*)64, NULL, (const void*)4096, (size_t)1 << 30, 1.0f,
+                             (uint16_t*)4096, (float*)8192, 0, (void*)256, (size_t)1 << 30,
+                             NULL) == KD_ERR_INVALID_ARG);
+  CHECK(kd_kl_backward_reuse(&p, NULL, (const uint16_t*)16, (const uint16_t*)16, NULL,
+                             (const float*)64, NULL, NULL, 0, 1.0f, (uint16_t*)4096, (float*)8192,
+                             0, (void*)256, (size_t)1 << 30, NULL) == KD_ERR_INVALID_ARG);
+
   CHECK(strcmp(kd_status_string(KD_OK), "KD_OK") == 0);
   CHECK(strcmp(kd_status_string(KD_ERR_TIMEOUT), "KD_ERR_TIMEOUT") == 0);
   CHECK(kd_launch_count() >= 0);

@@ -237,3 +237,35 @@ def test_topk_pointer_errors(lib):
     # the workspace grows linearly in T
     s = [kdkl.kd_lmhead_topk_workspace_size(t, 2880, 201088, 100) for t in (8192, 16384, 32768)]
     assert s[0] < s[1] < s[2] and abs((s[2] - s[1]) - 2 * (s[1] - s[0])) < (1 << 20)
+
+
+def test_backward_reuse_needs_a_known_forward_workspace(lib):
+    """kd_kl_backward_reuse reads the teacher rows a forward call prepared; a
+    workspace no forward filled for this problem is refused on the host,
+    before anything is queued (no device call happens here)."""
+    P = ctypes.c_void_p
+    p = kdkl.kd_kl_problem(10, 16, 100, 4, 1.0, 8)
+    need = lib.kd_kl_workspace_size(ctypes.byref(p), 4)
+    assert 0 < need < lib.kd_kl_workspace_size(ctypes.byref(p), 1)
+
+    def call(fwd_ws):
+        return lib.kd_kl_backward_reuse(ctypes.byref(p), None, P(16), P(16), None, P(64), None,
+                                        fwd_ws, 1 << 20, 1.0, P(4096), P(8192), 0, P(256),
+                                        need, None)
+    assert call(None) == 1            # KD_ERR_INVALID_ARG: no forward workspace
+    assert call(P(1 << 20)) == 1      # never filled by a forward call
+    # ordinary argument checks still come first
+    bad = kdkl.kd_kl_problem(10, 12, 100, 4, 1.0, 8)
+    assert lib.kd_kl_backward_reuse(ctypes.byref(bad), None, P(16), P(16), None, P(64), None,
+                                    P(1 << 20), 1 << 20, 1.0, P(4096), P(8192), 0, P(256), need,
+                                    None) == 3
+
+
+def test_binding_refuses_tensors_on_another_device():
+    """The binding runs each call with H's device current; a tensor elsewhere
+    is refused before anything is launched."""
+    import torch
+    a = torch.zeros(4, dtype=torch.uint8)
+    kdkl.same_device(a.device, x=a, y=None)
+    with pytest.raises(ValueError, match="expected"):
+        kdkl.same_device(a.device, x=torch.zeros(4, dtype=torch.uint8, device="meta"))

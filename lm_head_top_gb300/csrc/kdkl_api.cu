@@ -149,17 +149,17 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Split plan for the logit GEMMs (forward and backward recompute): how many
-// vocabulary splits per m-tile, and how many splits form one L2 group.
-// `num_sms` here counts unit processors (CTAs, or CTA pairs). A group keeps
-// G_m = num_sms / group_n m-tiles in flight; their A rows (tile_m x d bf16
-// each) must stay resident in L2 while the group's B tiles
-// stream past, so G_m is capped by kL2RowBudget. Among split counts that are
-// multiples of group_n, pick the one with the least waves x tiles per unit.
-struct SplitPlan {
-  int nsplit, group_n;
+// Unit plan of the logit GEMMs (forward, backward recompute, top-K). A unit is
+// one m-tile and one split of about `split_tiles` vocabulary tiles; units are
+// handed out while the kernel runs, in groups of group_m m-tiles with the
+// m-tile fastest (tc_gemm.cuh). The group's A rows (tile_m x d bf16 per
+// m-tile) stay in L2 while its splits stream past, so group_m is set by an
+// L2 budget for them. Short units keep the units in flight on a narrow window
+// of vocabulary tiles, which are then read from DRAM about once per group.
+struct LogitPlan {
+  int m_tiles, n_tiles, nsplit, group_m, units;
 };
-constexpr double kL2RowBudgetDefault = 24.0 * 1024 * 1024;
+constexpr double kL2RowBudgetDefault = 32.0 * 1024 * 1024;
 
 // KDKL_L2_ROWS_MB overrides the L2 budget for the A rows of one group (tuning).
 double l2_row_budget() {
@@ -168,40 +168,52 @@ double l2_row_budget() {
   return mb > 0 ? mb * 1024 * 1024 : kL2RowBudgetDefault;
 }
 
-SplitPlan choose_split(int m_tiles, int n_tiles, int num_sms, int64_t d, int tile_m) {
+// KDKL_SPLIT_TILES overrides the vocabulary tiles per unit of the forward
+// logit GEMM (tuning).
+int fwd_split_tiles() {
+  const char* v = getenv("KDKL_SPLIT_TILES");
+  const int n = v ? atoi(v) : 0;
+  return n > 0 ? n : 8;
+}
+
+LogitPlan plan_logit(int64_t rows, int64_t cols, int64_t d, int tile_m, int split_tiles) {
+  LogitPlan lp{};
+  lp.m_tiles = (int)std::max<int64_t>(ceil_div(rows, tile_m), 1);
+  lp.n_tiles = (int)ceil_div(cols, LOGIT_BN);
+  lp.nsplit = (int)std::max<int64_t>(1, ceil_div(lp.n_tiles, std::max(1, split_tiles)));
   const double a_tile_bytes = (double)tile_m * (double)d * 2.0;
-  int gm = (int)std::max(1.0, std::floor(l2_row_budget() / a_tile_bytes));
-  gm = std::min(gm, m_tiles);
-  int group_n = (num_sms + gm - 1) / gm;
-  group_n = std::max(1, std::min(group_n, n_tiles));
-  SplitPlan best{group_n, group_n};
-  double best_cost = 1e300;
-  for (int ns = group_n; ns <= n_tiles; ns += group_n) {
-    const int64_t units = (int64_t)m_tiles * ns;
-    const int64_t grid = std::min<int64_t>(units, num_sms);
-    const int64_t waves = ceil_div(units, grid);
-    const int64_t per_unit = ceil_div(n_tiles, ns);
-    const double cost = (double)waves * ((double)per_unit + 0.05);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best.nsplit = ns;
-    }
-  }
-  return best;
+  const int gm = (int)std::max(1.0, std::floor(l2_row_budget() / a_tile_bytes));
+  lp.group_m = std::min(gm, lp.m_tiles);
+  lp.units = lp.m_tiles * lp.nsplit;
+  return lp;
+}
+
+// KDKL_STATIC_SCHED=1: units are taken round-robin by CTA group instead of
+// from the launch counter (same order; kept to compare the two schedules).
+bool static_schedule() {
+  const char* v = getenv("KDKL_STATIC_SCHED");
+  return v && v[0] == '1';
 }
 
 struct FwdPlan {
   bool pair;
-  int m_tiles, n_tiles, nsplit, group_n, grid;
+  int m_tiles, n_tiles, nsplit, group_m, grid;
   size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_ps1, off_pzl, off_bsum, total;
 };
+
+// Per-launch unit counters live in the workspace header (ints from this
+// index on), zeroed with it at the start of every call.
+constexpr int kHeaderCounter0 = 16;
+constexpr int kHeaderCounters = 48;
 
 struct BwdPlan {
   bool vocab_slabs;  // true: blocks are all tokens x a vocabulary slab
   int64_t Tb, Vb;    // block extent (tokens, vocabulary)
   int64_t Tb_pad, Vb_pad;
   int64_t n_tblocks, n_vblocks;
-  size_t off_sidx, off_sp, off_G, off_dH, total;
+  // off_ctr: one unit counter per GEMM launch (3 per block), right after the
+  // header, zeroed with it at the start of every call
+  size_t off_ctr, off_sidx, off_sp, off_G, off_dH, total;
 };
 
 bool problem_ok(const kd_kl_problem* p) {
@@ -216,14 +228,15 @@ bool problem_ok(const kd_kl_problem* p) {
 }
 
 FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, bool mix = false) {
+  (void)num_sms;
   FwdPlan f{};
   const int tile_m = pair ? 2 * BM : BM;
   f.pair = pair;
-  f.m_tiles = (int)ceil_div(p.T, tile_m);
-  f.n_tiles = (int)ceil_div(p.V, LOGIT_BN);
-  const SplitPlan sp = choose_split(std::max(f.m_tiles, 1), f.n_tiles, procs, p.d, tile_m);
-  f.nsplit = p.T > 0 ? sp.nsplit : 1;
-  f.group_n = p.T > 0 ? sp.group_n : 1;
+  const LogitPlan lp = plan_logit(p.T, p.V, p.d, tile_m, fwd_split_tiles());
+  f.m_tiles = lp.m_tiles;
+  f.n_tiles = lp.n_tiles;
+  f.nsplit = p.T > 0 ? lp.nsplit : 1;
+  f.group_m = lp.group_m;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
   size_t o = kHeaderBytes;
   const size_t TK = (size_t)p.T * p.K;
@@ -265,6 +278,7 @@ BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
   b.Tb_pad = round_up(b.Tb, BM);
   b.Vb_pad = round_up(b.Vb, LOGIT_BN);
   size_t o = kHeaderBytes;
+  b.off_ctr = o; o = align256(o + (size_t)3 * b.n_tblocks * b.n_vblocks * 4);
   const size_t TK = own_teacher ? (size_t)p.T * p.K : 0;
   b.off_sidx = o; o = align256(o + TK * 4);
   b.off_sp = o; o = align256(o + TK * 4);
@@ -296,7 +310,7 @@ int topk_slack() {
 
 struct TopkPlan {
   bool pair;
-  int m_tiles, n_tiles, nsplit, group_n, grid, cap;
+  int m_tiles, n_tiles, nsplit, group_m, grid, cap;
   size_t off_cand, off_row_key, off_unit_val, off_unit_id, total;
 };
 
@@ -307,38 +321,20 @@ bool topk_problem_ok(const kd_topk_problem* p) {
 }
 
 TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) {
+  (void)num_sms;
   TopkPlan f{};
   const int tile_m = pair ? 2 * BM : BM;
   f.pair = pair;
-  f.m_tiles = (int)std::max<int64_t>(ceil_div(p.T, tile_m), 1);
-  f.n_tiles = (int)ceil_div(p.V, LOGIT_BN);
-  SplitPlan sp = choose_split(f.m_tiles, f.n_tiles, procs, p.d, tile_m);
-  const int max_ns = std::max(1, std::min(f.n_tiles, kTopkMergeMax / p.K));
-  if (sp.nsplit > max_ns) {
-    sp.nsplit = max_ns;
-    sp.group_n = std::min(sp.group_n, max_ns);
-  }
-  f.nsplit = sp.nsplit;
-  // Fewer splits of a row in flight than the logit GEMMs use: a split that
-  // starts after another split of its rows has compacted begins from the
-  // threshold that split published, so it appends and compacts far less.
-  // Bounded by L2 room for the A rows of the m-tiles in flight (~half of L2).
-  // At the GPT-OSS-like head, 2 instead of 5 cut the kernel's cycles by 9 %.
-  f.group_n = sp.group_n;
-  // With the first-split phase (at least as many m-tiles as processors; see
-  // kd_lmhead_topk) the rows' thresholds are set before the groups start, and
-  // 3 splits in flight measured faster than 2 at 32K tokens (fewer W
-  // re-reads): 25.1 vs 25.8 ms, 5 splits 25.5 (3 alternating rounds).
-  {
-    const double a_tile = (double)tile_m * (double)p.d * 2.0;
-    int g = f.m_tiles >= procs ? 3 : 2;
-    while (g < sp.group_n && ceil_div(procs, g) * a_tile > 64.0 * 1024 * 1024) ++g;
-    f.group_n = std::min(sp.group_n, g);
-  }
-  if (const char* g = getenv("KDKL_TOPK_GROUP")) {  // tuning: splits in flight per m-tile
-    const int gn = atoi(g);
-    if (gn > 0) f.group_n = std::min(gn, f.nsplit);
-  }
+  const int n_tiles = (int)ceil_div(p.V, LOGIT_BN);
+  // Short units as in the forward (about 16 vocabulary tiles), but never more
+  // than kTopkMergeMax entries per row for the merge (nsplit * K).
+  int st = std::max<int>(16, (int)ceil_div((int64_t)n_tiles * p.K, kTopkMergeMax));
+  while (ceil_div(n_tiles, st) * p.K > kTopkMergeMax && st < n_tiles) ++st;
+  const LogitPlan lp = plan_logit(p.T, p.V, p.d, tile_m, st);
+  f.m_tiles = lp.m_tiles;
+  f.n_tiles = lp.n_tiles;
+  f.nsplit = lp.nsplit;
+  f.group_m = lp.group_m;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
   f.cap = std::max(p.K + 64, std::min(512, p.K + topk_slack()));
   // two list banks per (CTA, row), any grid <= SMs
@@ -372,9 +368,9 @@ bool log_plan() {
 void print_plan(const char* what, bool pair, int procs, const GemmShape& sh, int grid) {
   fprintf(stderr,
           "[kdkl] %s pair=%d procs=%d max_clusters=%d m_tiles=%d n_tiles=%d nsplit=%d "
-          "group_n=%d units=%d k_blocks=%d grid=%d\n",
+          "group_m=%d units=%d k_blocks=%d grid=%d dynamic=%d\n",
           what, pair ? 1 : 0, procs, pair ? pair_max_active_clusters() : 0, sh.m_tiles,
-          sh.n_tiles, sh.nsplit, sh.group_n, sh.units, sh.k_blocks, grid);
+          sh.n_tiles, sh.nsplit, sh.group_m, sh.units, sh.k_blocks, grid, sh.counter ? 1 : 0);
 }
 
 // Unit processors of the persistent GEMM grid: CTAs, or co-resident CTA pairs.
@@ -578,9 +574,10 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
   sh.m_tiles = f.m_tiles;
   sh.n_tiles = f.n_tiles;
   sh.nsplit = f.nsplit;
-  sh.group_n = f.group_n;
+  sh.group_m = f.group_m;
   sh.units = f.m_tiles * f.nsplit;
   sh.k_blocks = (int)ceil_div(d, BK);
+  sh.counter = static_schedule() ? nullptr : status + kHeaderCounter0;
   EpiParams ep{};
   ep.sidx = sidx;
   ep.sp = sp;
@@ -671,7 +668,10 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   int* status = at<int>(workspace, 0);
   // the counted-token total N: this call's own, or the forward's
   int* n_count = reuse ? const_cast<int*>(static_cast<const int*>(fwd_ws)) + 1 : status + 1;
-  KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
+  KD_CUDA(cudaMemsetAsync(workspace, 0, b.off_sidx, stream));  // header and unit counters
+  int* counters = static_schedule() ? nullptr : at<int>(workspace, b.off_ctr);
+  int launch_no = 0;  // index of the next GEMM launch's counter
+  auto next_counter = [&]() { return counters ? counters + launch_no++ : nullptr; };
   if (p.T == 0) {
     if (!accumulate_dW) KD_CUDA(cudaMemsetAsync(dW, 0, (size_t)p.V * p.d * 4, stream));
     return KD_OK;
@@ -679,11 +679,12 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
   const float inv_tau = 1.0f / p.temperature;
   const float cl2 = 1.4426950408889634f * inv_tau;
-  // Sorted teacher ids and probabilities: the forward workspace's (same
-  // offsets in both layouts), or prepared here.
-  void* tws = reuse ? const_cast<void*>(fwd_ws) : workspace;
-  int32_t* sidx = at<int32_t>(tws, b.off_sidx);
-  float* sp = at<float>(tws, b.off_sidx + align256((size_t)p.T * p.K * 4));
+  // Sorted teacher ids and probabilities: the forward workspace's (right
+  // after its header), or prepared here.
+  void* fws = const_cast<void*>(fwd_ws);
+  int32_t* sidx = reuse ? at<int32_t>(fws, kHeaderBytes) : at<int32_t>(workspace, b.off_sidx);
+  float* sp = reuse ? at<float>(fws, kHeaderBytes + align256((size_t)p.T * p.K * 4))
+                    : at<float>(workspace, b.off_sp);
   uint16_t* Gbuf = at<uint16_t>(workspace, b.off_G);
   float* dH_acc = at<float>(workspace, b.off_dH);
 
@@ -717,17 +718,21 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
 
       // 1) recompute the logits of the block and store (softmax - P) * m g / (tau N)
       {
+        // Units of 2 vocabulary tiles: nothing runs across tiles but each
+        // row's cursor into its teacher ids, and short units keep the tail
+        // of these short launches small.
+        const LogitPlan lp = plan_logit(rows, cols, d, tile_m, 2);
         GemmShape sh{};
         sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(rows, tile_m);
-        sh.n_tiles = (int)ceil_div(cols, LOGIT_BN);
-        const SplitPlan spl = choose_split(sh.m_tiles, sh.n_tiles, procs, d, tile_m);
-        sh.nsplit = spl.nsplit;
-        sh.group_n = spl.group_n;
-        sh.units = sh.m_tiles * sh.nsplit;
+        sh.m_tiles = lp.m_tiles;
+        sh.n_tiles = lp.n_tiles;
+        sh.nsplit = lp.nsplit;
+        sh.group_m = lp.group_m;
+        sh.units = lp.units;
         sh.k_blocks = (int)ceil_div(d, BK);
         sh.a_m0 = row0;
         sh.b_n0 = col0;
+        sh.counter = next_counter();
         EpiParams ep{};
         ep.sidx = sidx;
         ep.sp = sp;
@@ -766,10 +771,11 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         sh.m_tiles = (int)ceil_div(rows, tile_m);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
-        sh.group_n = dn_tiles;
+        sh.group_m = 1;  // m-major: an m-tile's output tiles run side by side
         sh.units = sh.m_tiles * sh.nsplit;
         sh.k_blocks = (int)ceil_div(cols, BK);
         sh.b_k0 = col0;
+        sh.counter = next_counter();
         EpiParams ep{};
         ep.out = dH_acc + (int64_t)row0 * d;
         ep.ldo = d;
@@ -789,10 +795,11 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         sh.m_tiles = (int)ceil_div(cols, tile_m);
         sh.n_tiles = dn_tiles;
         sh.nsplit = dn_tiles;
-        sh.group_n = dn_tiles;
+        sh.group_m = 1;
         sh.units = sh.m_tiles * sh.nsplit;
         sh.k_blocks = (int)ceil_div(rows, BK);
         sh.b_k0 = row0;
+        sh.counter = next_counter();
         EpiParams ep{};
         ep.out = dW + (int64_t)col0 * d;
         ep.ldo = d;
@@ -958,9 +965,10 @@ kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const u
   sh.m_tiles = f.m_tiles;
   sh.n_tiles = f.n_tiles;
   sh.nsplit = f.nsplit;
-  sh.group_n = f.group_n;
+  sh.group_m = f.group_m;
   sh.units = f.m_tiles * f.nsplit;
   sh.k_blocks = (int)ceil_div(d, BK);
+  sh.counter = static_schedule() ? nullptr : status + kHeaderCounter0;
   EpiParams ep{};
   ep.K = K;
   ep.T = T;

@@ -57,8 +57,8 @@ struct TileCfg {
   static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
-  // full, empty, tmem full x2, tmem empty x2, drain
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // full, empty, tmem full x2, tmem empty x2, drain, unit-slot full / empty
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * 4;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 512;
 };
 
@@ -66,14 +66,16 @@ enum { EPI_LSE = 0, EPI_GRAD = 1, EPI_STORE = 2, EPI_TOPK = 3, EPI_LSE_MIX = 4, 
 
 // Work decomposition: `units` = m_tiles * nsplit. A unit is one m-tile and one
 // split (a contiguous range of n-tiles). Units are numbered group by group:
-// the splits form groups of `group_n`; inside a group the split index runs
-// fastest, then the m-tile. Consecutive units (the ones in flight together on
-// the persistent CTAs) therefore cover ~num_CTAs/group_n m-tiles x group_n
-// splits: the A rows of those m-tiles stay in L2 while every B tile is fetched
-// from DRAM once per pass of such a group. group_n == nsplit gives plain
-// m-major order.
+// the m-tiles form groups of `group_m`; inside a group the m-tile runs
+// fastest, then the split. Units are handed out in that order while the
+// kernel runs (an atomic counter; see `counter`), so the units in flight at
+// any moment are a window of consecutive numbers: a few splits of one group's
+// m-tiles. Their B tiles are read from DRAM about once per group and their
+// A rows (group_m m-tiles) stay in L2 for the group's duration, however the
+// CTAs' speeds differ. group_m == 1 gives m-major order (every split of an
+// m-tile, then the next m-tile).
 struct GemmShape {
-  int m_tiles, n_tiles, nsplit, group_n, units;
+  int m_tiles, n_tiles, nsplit, group_m, units;
   int k_blocks;
   int a_m0, a_k0;  // A coordinate offsets (rows M / reduction K)
   int b_n0, b_k0;  // B coordinate offsets (rows N / reduction K)
@@ -81,13 +83,17 @@ struct GemmShape {
   // warp's first wait runs out (after kInjectedWaitLimitNs) and the block
   // unwinds through its error path. Never set in normal calls.
   int inject_stall;
-  // When > 0, the first group holds only this many splits (the rest use
-  // group_n): the top-K producer runs one split of every row first, so that
-  // the row's other splits start from the threshold it publishes.
+  // Nonzero: split 0 of every m-tile runs first (units 0 .. m_tiles-1), then
+  // the groups over splits 1.. . The top-K producer uses it so that a row's
+  // other splits start from the threshold its first split published.
   int first_group;
-  // When > 0 (with first_group == 1): split 0 covers n-tiles [0, first_ntiles)
+  // When > 0 (with first_group): split 0 covers n-tiles [0, first_ntiles)
   // and splits 1.. share the rest evenly; 0: every split gets an even share.
   int first_ntiles;
+  // Unit counter for this launch (zero before it starts): the leader CTA's
+  // producer takes the next unit with atomicAdd. nullptr: static round-robin
+  // (CTA group g takes units g, g + groups, ...), kept to compare schedules.
+  int* counter;
 };
 
 // n-tile range [nb, ne) of split s.
@@ -258,24 +264,25 @@ __device__ __forceinline__ float topk_shared_threshold(const uint32_t* row_key) 
 
 __device__ __forceinline__ void unit_coords(const GemmShape& sh, int u, int& m, int& s, int& nb,
                                             int& ne) {
-  int s_base = 0;
-  if (sh.first_group > 0) {
-    const int fg_units = sh.m_tiles * sh.first_group;
-    if (u < fg_units) {
-      m = u / sh.first_group;
-      s = u - m * sh.first_group;
-      split_range(sh, s, nb, ne);
+  int s0 = 0;
+  if (sh.first_group) {
+    if (u < sh.m_tiles) {
+      m = u;
+      s = 0;
+      split_range(sh, 0, nb, ne);
       return;
     }
-    u -= fg_units;
-    s_base = sh.first_group;
+    u -= sh.m_tiles;
+    s0 = 1;
   }
-  const int per_group = sh.m_tiles * sh.group_n;
+  const int ns = sh.nsplit - s0;
+  const int per_group = sh.group_m * ns;
   const int g = u / per_group;
   const int r = u - g * per_group;
-  const int gsize = min(sh.group_n, sh.nsplit - s_base - g * sh.group_n);  // last may be short
-  m = r / gsize;
-  s = s_base + g * sh.group_n + (r - m * gsize);
+  const int gm = min(sh.group_m, sh.m_tiles - g * sh.group_m);  // the last group may be short
+  const int si = r / gm;
+  s = s0 + si;
+  m = g * sh.group_m + (r - si * gm);
   split_range(sh, s, nb, ne);
 }
 
@@ -311,6 +318,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Ring of units handed from the scheduler (the leader CTA's producer) to
+  // every other role of both CTAs: slot i holds a unit number (-1: no more).
+  constexpr int NSLOT = 4;
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -318,6 +329,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto ufull_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + i); };
+  auto uempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + NSLOT + i); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -338,6 +351,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty_bar(b), PAIR ? 8 : 4);
     }
     mbar_init(drain_bar, 1);
+    // A slot is released by every role that reads it: the MMA thread and the
+    // 4 epilogue warps here, and with a pair the peer's producer and its 4
+    // epilogue warps (remote arrives on the leader's barrier).
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(ufull_bar(i), 1);
+      mbar_init(uempty_bar(i), PAIR ? 10 : 5);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -359,6 +379,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Consumer side of the unit ring: wait for slot q's unit (cluster-scope
+  // acquire with a pair: the leader wrote the peer's slot remotely), then
+  // release the slot on the leader's barrier once the value is read.
+  const uint32_t uempty_leader0 = PAIR ? mapa_shared(uempty_bar(0), 0) : uempty_bar(0);
+  auto take_unit = [&](int q, int& u) -> bool {
+    const int slot = q & (NSLOT - 1);
+    const uint32_t ph = (uint32_t)(q / NSLOT) & 1u;
+    const bool got = PAIR ? mbar_wait_cluster_bounded(ufull_bar(slot), ph, abort_flag, status, limit)
+                          : mbar_wait_bounded(ufull_bar(slot), ph, abort_flag, status, limit);
+    if (got) u = unit_slot[slot];
+    return got;
+  };
+  auto release_unit = [&](int q) {
+    const int slot = q & (NSLOT - 1);
+    if (PAIR)
+      mbar_arrive_cluster(uempty_leader0 + 8u * slot);
+    else
+      mbar_arrive(uempty_bar(slot));
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
@@ -372,7 +412,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       long long fills = 0;
       bool ok = sh.inject_stall == 0;
       const uint32_t full_leader0 = PAIR ? mapa_shared(full_bar(0), 0) : full_bar(0);
-      for (int u = group0; ok && u < sh.units; u += groups) {
+      // The leader's producer is also the scheduler: it takes units from the
+      // launch's counter (the next one fetched a unit ahead, so the atomic's
+      // latency hides behind a unit of copies) and publishes each in the ring.
+      const bool dyn = sh.counter != nullptr;
+      int next = (ok && leader) ? (dyn ? atomicAdd(sh.counter, 1) : group0) : -1;
+      const uint32_t peer_slot0 = PAIR ? mapa_shared(smem_u32((const void*)unit_slot), 1) : 0u;
+      const uint32_t peer_ufull0 = PAIR ? mapa_shared(ufull_bar(0), 1) : 0u;
+      for (int uq = 0; ok; ++uq) {
+        int u = -1;
+        if (leader) {
+          const int slot = uq & (NSLOT - 1);
+          const uint32_t ph = ((uint32_t)(uq / NSLOT) & 1u) ^ 1u;
+          const bool freed =
+              PAIR ? mbar_wait_cluster_bounded(uempty_bar(slot), ph, abort_flag, status, limit)
+                   : mbar_wait_bounded(uempty_bar(slot), ph, abort_flag, status, limit);
+          if (!freed) {
+            ok = false;
+            break;
+          }
+          u = next < sh.units ? next : -1;
+          if (u >= 0) next = dyn ? atomicAdd(sh.counter, 1) : next + groups;
+          unit_slot[slot] = u;
+          if (PAIR) {
+            st_shared_cluster_u32(peer_slot0 + 4u * slot, (uint32_t)u);
+            mbar_arrive_cluster(peer_ufull0 + 8u * slot);
+          }
+          mbar_arrive(ufull_bar(slot));
+        } else {
+          if (!take_unit(uq, u)) {
+            ok = false;
+            break;
+          }
+          release_unit(uq);
+        }
+        if (u < 0) break;
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         const int a_row = sh.a_m0 + m * TILE_M + (int)rank * BM;
@@ -434,7 +508,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = group0; ok && u < sh.units; u += groups) {
+      for (int uq = 0; ok; ++uq) {
+        int u = -1;
+        if (!take_unit(uq, u)) break;
+        release_unit(uq);
+        if (u < 0) break;
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
@@ -528,7 +606,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         ep.unit_id[o + k] = __float_as_int(c.y);
       }
     };
-    for (int u = group0; ok && u < sh.units; u += groups) {
+    for (int uq = 0; ok; ++uq) {  // uq: position in the unit ring (q is the lane quarter)
+      int u = -1;
+      const bool got_unit = __all_sync(0xffffffffu, take_unit(uq, u));
+      if (!got_unit) {
+        ok = false;
+        break;
+      }
+      __syncwarp();  // every lane has read the slot before it is released
+      if (lane == 0) release_unit(uq);
+      if (u < 0) break;
       int m, s, nb, ne;
       unit_coords(sh, u, m, s, nb, ne);
       const int r = m * TILE_M + (int)rank * BM + r_in_tile;  // row within this launch

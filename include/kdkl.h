@@ -257,7 +257,7 @@ kd_status kd_rkl_backward(const kd_kl_problem* prob, const uint16_t* H, const ui
  * tensor-core GEMM produces each logit tile; its epilogue keeps per-row
  * candidate lists above a running threshold, so the logits are never stored.
  */
-#define KDKL_TOPK_MAX_K 256
+#define KDKL_TOPK_MAX_K 512
 
 typedef struct {
   int64_t T;   /* rows of H (tokens) */

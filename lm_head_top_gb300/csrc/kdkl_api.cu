@@ -291,7 +291,9 @@ BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
 // ---- offline top-K producer
 
 
-constexpr int kTopkMergeMax = 4096;  // nsplit * K entries sorted per row by the merge
+// nsplit * K at most: bounds the per-split lists in the workspace (8 bytes per
+// entry per row: 128 KB per token at this size)
+constexpr int kTopkMergeMax = 4096;
 // 256: measured faster than 512 (24.86/24.89 vs 25.38/25.23 ms at 32K tokens,
 // alternating) and than 128 (26.2) once the first split sets the thresholds;
 // smaller lists also leave more of L2 to the operand tiles.
@@ -311,7 +313,7 @@ int topk_slack() {
 struct TopkPlan {
   bool pair;
   int m_tiles, n_tiles, nsplit, group_m, grid, cap;
-  size_t off_cand, off_row_key, off_unit_val, off_unit_id, total;
+  size_t off_cand, off_row_key, off_unit_val, off_unit_id, off_unit_cnt, total;
 };
 
 bool topk_problem_ok(const kd_topk_problem* p) {
@@ -326,9 +328,15 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   const int tile_m = pair ? 2 * BM : BM;
   f.pair = pair;
   const int n_tiles = (int)ceil_div(p.V, LOGIT_BN);
-  // Short units as in the forward (about 16 vocabulary tiles), but never more
-  // than kTopkMergeMax entries per row for the merge (nsplit * K).
-  int st = std::max<int>(16, (int)ceil_div((int64_t)n_tiles * p.K, kTopkMergeMax));
+  // Units of about 48 vocabulary tiles (KDKL_TOPK_SPLIT_TILES overrides; a
+  // split's K-th logit, the threshold it publishes for its rows, is the
+  // sharper the wider the split, and the fewer entries reach the merge:
+  // measured at 32K tokens, merge 2.08 / 1.71 / 1.03 / 0.47 ms for 16 / 32 /
+  // 48 / 80 tiles with the GEMM within noise, 48 and 80 best in total), but
+  // never more than kTopkMergeMax list entries per row (nsplit * K).
+  const char* stv = getenv("KDKL_TOPK_SPLIT_TILES");
+  const int st0 = stv && atoi(stv) > 0 ? atoi(stv) : 48;
+  int st = std::max<int>(st0, (int)ceil_div((int64_t)n_tiles * p.K, kTopkMergeMax));
   while (ceil_div(n_tiles, st) * p.K > kTopkMergeMax && st < n_tiles) ++st;
   const LogitPlan lp = plan_logit(p.T, p.V, p.d, tile_m, st);
   f.m_tiles = lp.m_tiles;
@@ -336,7 +344,7 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   f.nsplit = lp.nsplit;
   f.group_m = lp.group_m;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
-  f.cap = std::max(p.K + 64, std::min(512, p.K + topk_slack()));
+  f.cap = std::max(p.K + 64, std::min(1024, p.K + topk_slack()));
   // two list banks per (CTA, row), any grid <= SMs
   const size_t cand = (size_t)num_sms * BM * 2 * f.cap;
   const size_t unit = (size_t)f.nsplit * p.T * p.K;
@@ -345,6 +353,7 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   f.off_row_key = o; o = align256(o + (size_t)p.T * 4);
   f.off_unit_val = o; o = align256(o + unit * 4);
   f.off_unit_id = o; o = align256(o + unit * 4);
+  f.off_unit_cnt = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
   f.total = o;
   return f;
 }
@@ -995,9 +1004,11 @@ kd_status kd_lmhead_topk(const kd_topk_problem* prob, const uint16_t* H, const u
   KD_CUDA(cudaMemsetAsync(ep.row_key, 0, (size_t)T * 4, stream));
   ep.unit_val = at<float>(workspace, f.off_unit_val);
   ep.unit_id = at<int32_t>(workspace, f.off_unit_id);
+  ep.unit_cnt = at<int>(workspace, f.off_unit_cnt);
   if (log_plan()) print_plan("topk", pair, procs, sh, f.grid);
   KD_CUDA(launch_gemm(GEMM_TOPK, LOGIT_BN, pair, tmH, tmW, sh, ep, status, f.grid, stream));
-  KD_CUDA(launch_topk_merge(ep.unit_val, ep.unit_id, ep.row_key, f.nsplit, T, K, topk_idx,
+  KD_CUDA(launch_topk_merge(ep.unit_val, ep.unit_id, ep.unit_cnt, ep.row_key, f.nsplit, T, K,
+                            topk_idx,
                             topk_logit, stream));
   return KD_OK;
 }

@@ -74,9 +74,9 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int 
                                cudaStream_t stream);
 // merge of per-split top-K lists; shared memory = topk_merge_p2() * 8 bytes
 int topk_merge_p2(int nsplit, int K);
-cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const uint32_t* row_key,
-                              int nsplit, int T, int K, int32_t* out_id, float* out_val,
-                              cudaStream_t stream);
+cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const int* unit_cnt,
+                              const uint32_t* row_key, int nsplit, int T, int K, int32_t* out_id,
+                              float* out_val, cudaStream_t stream);
 
 // kernels_rkl.cu — reverse KL over the cached ids (CUDA cores; see the file)
 struct RklLayout {

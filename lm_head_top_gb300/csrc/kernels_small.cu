@@ -428,44 +428,75 @@ __device__ int merge_select_k(unsigned long long* keys, int m, int K) {
 }
 
 // One warp per row; `rows_per_block` warps share the block's shared memory,
-// cap entries (a power of two >= nsplit * K) each.
+// cap entries each (a power of two, at least K + 32). Split s of row t kept
+// unit_cnt[s, t] entries (at most K) at the start of its [s, t] slot.
 __global__ void __launch_bounds__(256)
     topk_merge_kernel(const float* __restrict__ unit_val, const int32_t* __restrict__ unit_id,
-                      const uint32_t* __restrict__ row_key, int nsplit, int T, int K, int cap,
-                      int32_t* __restrict__ out_id, float* __restrict__ out_val) {
+                      const int* __restrict__ unit_cnt, const uint32_t* __restrict__ row_key,
+                      int nsplit, int T, int K, int cap, int32_t* __restrict__ out_id,
+                      float* __restrict__ out_val) {
   extern __shared__ unsigned long long mkeys_all[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;  // whole warp leaves together; no block-wide barrier below
   unsigned long long* mkeys = mkeys_all + (size_t)warp * cap;
-  const int n = nsplit * K;
   const uint32_t floor_key = row_key[t];
   const uint32_t below = (1u << lane) - 1u;
   int m = 0;
-  constexpr int BATCH = 8;  // independent loads in flight per lane
-  for (int e0 = 0; e0 < n; e0 += 32 * BATCH) {
-    float vb[BATCH];
-    int32_t ib[BATCH];
+  unsigned long long cut = ~0ull;  // every kept key is below it
+  constexpr int BATCH = 8;  // splits whose entries are loaded together
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int c_lane = s0 + lane < nsplit ? min(unit_cnt[(long long)(s0 + lane) * T + t], K) : 0;
+    const int nb = min(32, nsplit - s0);
+    for (int j0 = 0; j0 < nb; j0 += BATCH) {
+      // the first 32 entries of BATCH splits in flight at once; longer lists
+      // (up to K) are finished split by split below
+      float vb[BATCH];
+      int32_t ib[BATCH];
+      int cb[BATCH];
 #pragma unroll
-    for (int b = 0; b < BATCH; ++b) {
-      const int e = e0 + b * 32 + lane;
-      if (e < n) {
-        const int s = e / K, k = e - s * K;
-        const long long o = ((long long)s * T + t) * K + k;
-        vb[b] = unit_val[o];
-        ib[b] = unit_id[o];
-      } else {
-        vb[b] = -INFINITY;
-        ib[b] = -1;
+      for (int b = 0; b < BATCH; ++b) {
+        cb[b] = __shfl_sync(0xffffffffu, c_lane, (j0 + b) & 31);
+        if (j0 + b >= nb) cb[b] = 0;
+        const long long o = ((long long)(s0 + j0 + b) * T + t) * K + lane;
+        vb[b] = lane < cb[b] ? unit_val[o] : -INFINITY;
+        ib[b] = lane < cb[b] ? unit_id[o] : -1;
       }
-    }
 #pragma unroll
-    for (int b = 0; b < BATCH; ++b) {
-      const uint32_t ok = merge_order_key(vb[b]);
-      const bool keep = ib[b] >= 0 && ok >= floor_key;
-      const uint32_t mask = __ballot_sync(0xffffffffu, keep);
-      if (keep) mkeys[m + __popc(mask & below)] = ((unsigned long long)(~ok) << 32) | (uint32_t)ib[b];
-      m += __popc(mask);
+      for (int b = 0; b < BATCH; ++b) {
+        for (int k0 = 0; k0 < cb[b]; k0 += 32) {
+          float v = vb[b];
+          int32_t id = ib[b];
+          if (k0 > 0) {
+            const long long o = ((long long)(s0 + j0 + b) * T + t) * K + k0 + lane;
+            v = k0 + lane < cb[b] ? unit_val[o] : -INFINITY;
+            id = k0 + lane < cb[b] ? unit_id[o] : -1;
+          }
+          const uint32_t ok = merge_order_key(v);
+          const unsigned long long key = ((unsigned long long)(~ok) << 32) | (uint32_t)id;
+          const bool keep = id >= 0 && ok >= floor_key && key < cut;
+          // A full buffer keeps only its K best before taking more (ids are
+          // distinct within a row, as merge_select_k needs); the largest of
+          // those K keys then bounds every later entry: one with a larger key
+          // (a smaller logit, or the same logit and a larger id) cannot enter.
+          if (m + 32 > cap) {
+            __syncwarp();
+            m = merge_select_k(mkeys, m, K);
+            unsigned long long mx = 0ull;
+            for (int e = lane; e < m; e += 32) mx = mkeys[e] > mx ? mkeys[e] : mx;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const unsigned long long y = __shfl_xor_sync(0xffffffffu, mx, o);
+              mx = y > mx ? y : mx;
+            }
+            cut = mx;
+          }
+          const bool take = keep && key < cut;
+          const uint32_t mask = __ballot_sync(0xffffffffu, take);
+          if (take) mkeys[m + __popc(mask & below)] = key;
+          m += __popc(mask);
+        }
+      }
     }
   }
   __syncwarp();
@@ -572,20 +603,23 @@ cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const in
                        block_sums, nblocks, n_count, loss);
 }
 
+// Merge buffer entries per row: room for every split's list when that is at
+// most 2048 entries, else 2048 (the buffer is cut back to the K best when full).
 int topk_merge_p2(int nsplit, int K) {
-  int p2 = 1;
-  while (p2 < nsplit * K) p2 <<= 1;
-  return p2 < 2 ? 2 : p2;
+  int p2 = 64;
+  while (p2 < nsplit * K && p2 < 2048) p2 <<= 1;
+  while (p2 < K + 32) p2 <<= 1;
+  return p2;
 }
 
-cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const uint32_t* row_key,
-                              int nsplit, int T, int K, int32_t* out_id, float* out_val,
-                              cudaStream_t stream) {
-  const int cap = topk_merge_p2(nsplit, K);  // <= 4096 entries, 32 KB per warp
+cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const int* unit_cnt,
+                              const uint32_t* row_key, int nsplit, int T, int K, int32_t* out_id,
+                              float* out_val, cudaStream_t stream) {
+  const int cap = topk_merge_p2(nsplit, K);  // <= 2048 entries, 16 KB per warp
   const int warps = std::max(1, std::min(8, 6144 / cap));  // <= 48 KB of shared memory
   return launch_kernel("topk_merge", topk_merge_kernel, dim3((T + warps - 1) / warps),
                        dim3(32 * warps), (size_t)warps * cap * sizeof(unsigned long long), stream,
-                       unit_val, unit_id, row_key, nsplit, T, K, cap, out_id, out_val);
+                       unit_val, unit_id, unit_cnt, row_key, nsplit, T, K, cap, out_id, out_val);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,

@@ -149,11 +149,12 @@ struct EpiParams {
   float kl_weight;        // alpha * c / tau (times g / N per counted row) (GRAD_MIX)
   float ce_weight;        // (1 - alpha)     (times g / N per counted row) (GRAD_MIX)
   // EPI_TOPK (K is the field above)
-  int topk_cap;      // capacity of a row's candidate list (K + 256, at most 512)
+  int topk_cap;      // capacity of a row's candidate list (K + slack, at most 1024)
   float2* cand;      // [gridDim.x * BM, topk_cap] (logit, id bits), one list per (CTA, row)
   uint32_t* row_key; // [T] order key of the best K-th logit any split has seen (0 = none)
-  float* unit_val;   // [nsplit, T, K] each split's top-K per row (id order)
+  float* unit_val;   // [nsplit, T, K] each split's kept top-K entries per row (id order)
   int32_t* unit_id;
+  int* unit_cnt;     // [nsplit, T] entries kept per (split, row)
 };
 
 // Order-preserving map of an fp32 value to uint32 (larger float, larger key).
@@ -166,15 +167,15 @@ __device__ __forceinline__ float f32_from_order_key(uint32_t k) {
 }
 
 // The whole warp reduces one row's candidate list (n entries, n >= K, at most
-// 512, appended in increasing id order) to its K best by (logit descending, id
-// ascending), in place and in the same id order. Returns the K-th best logit,
+// 32 * MAXE, appended in increasing id order) to its K best by (logit
+// descending, id ascending), in place and in the same id order. Returns the K-th best logit,
 // the row's new admission threshold: a later candidate of the same row has a
 // larger id, so only a strictly larger logit can displace a kept entry.
 // The K-th largest key is found by bisection over the 32-bit order keys,
 // starting from the list's min/max keys and stopping early once a midpoint
 // separates exactly K keys.
-static __device__ __noinline__ float topk_compact_row(float2* list, int n, int K) {
-  constexpr int MAXE = 16;  // 512 entries / 32 lanes
+template <int MAXE>
+static __device__ __noinline__ float topk_compact_row_n(float2* list, int n, int K) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
   uint32_t key[MAXE];
@@ -252,6 +253,12 @@ static __device__ __noinline__ float topk_compact_row(float2* list, int n, int K
   }
   __syncwarp();
   return f32_from_order_key(lo);
+}
+
+// Lists of up to 512 entries (K <= 256 with the default slack) take the
+// 16-slot form; longer ones (K up to 512) the 32-slot form.
+__device__ __forceinline__ float topk_compact_row(float2* list, int n, int K, int cap) {
+  return cap <= 512 ? topk_compact_row_n<16>(list, n, K) : topk_compact_row_n<32>(list, n, K);
 }
 
 // Admission threshold from the best K-th logit published by any split of the
@@ -594,17 +601,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int ni = __shfl_sync(0xffffffffu, pend_cnt, i);
       float2* li = list_of(i, pend_bank);
       if (ni > ep.K) {
-        const float thi = topk_compact_row(li, ni, ep.K);
+        const float thi = topk_compact_row(li, ni, ep.K, ep.topk_cap);
         if (lane == 0) atomicMax(ep.row_key + ep.row0 + pend_r0 + i, f32_order_key(thi));
       }
       __syncwarp();
+      // Only entries at or above the row's best published K-th logit can be
+      // in its top-K: the rest are dropped here, the kept ones written in
+      // order with their count, so the merge reads only what survives.
+      const long long row = (long long)ep.row0 + pend_r0 + i;
+      const float th_now = topk_shared_threshold(ep.row_key + row);
       const int nk = min(ni, ep.K);
-      const long long o = ((long long)pend_s * ep.T + ep.row0 + pend_r0 + i) * ep.K;
-      for (int k = lane; k < ep.K; k += 32) {
-        const float2 c = k < nk ? li[k] : make_float2(-INFINITY, __int_as_float(-1));
-        ep.unit_val[o + k] = c.x;
-        ep.unit_id[o + k] = __float_as_int(c.y);
+      const long long o = ((long long)pend_s * ep.T + row) * ep.K;
+      const uint32_t below = (1u << lane) - 1u;
+      int w = 0;
+      for (int k0 = 0; k0 < nk; k0 += 32) {
+        const int k = k0 + lane;
+        const float2 c = k < nk ? li[k] : make_float2(-INFINITY, 0.f);
+        const bool keep = k < nk && c.x > th_now;
+        const uint32_t km = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          ep.unit_val[o + w + __popc(km & below)] = c.x;
+          ep.unit_id[o + w + __popc(km & below)] = __float_as_int(c.y);
+        }
+        w += __popc(km);
       }
+      if (lane == 0) ep.unit_cnt[(long long)pend_s * ep.T + row] = w;
     };
     for (int uq = 0; ok; ++uq) {  // uq: position in the unit ring (q is the lane quarter)
       int u = -1;
@@ -684,7 +705,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (!want) break;
             const int i = __ffs(want) - 1;
             const int ni = __shfl_sync(0xffffffffu, cnt, i);
-            const float thi = topk_compact_row(list_of(i, bank), ni, ep.K);
+            const float thi = topk_compact_row(list_of(i, bank), ni, ep.K, ep.topk_cap);
             if (lane == i) {
               th = fmaxf(th, thi);
               cnt = ep.K;
@@ -715,7 +736,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const int i = __ffs(need) - 1;
               need &= need - 1u;
               const int ni = __shfl_sync(0xffffffffu, cnt, i);
-              const float thi = topk_compact_row(list_of(i, bank), ni, ep.K);
+              const float thi = topk_compact_row(list_of(i, bank), ni, ep.K, ep.topk_cap);
               if (lane == i) {
                 th = fmaxf(th, thi);
                 cnt = ep.K;

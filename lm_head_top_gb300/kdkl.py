@@ -46,7 +46,7 @@ class kd_topk_problem(ctypes.Structure):
                 ("K", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
-KDKL_TOPK_MAX_K = 256
+KDKL_TOPK_MAX_K = 512
 
 
 class kd_kernel_time(ctypes.Structure):

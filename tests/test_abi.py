@@ -212,12 +212,13 @@ def _topk(lib, p, H=16, W=16, idx=64, val=128, ws=256, ws_bytes=1 << 30):
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("K", 0, 2), ("K", 257, 2),          # 1..KDKL_TOPK_MAX_K
+    ("K", 0, 2), ("K", 513, 2),          # 1..KDKL_TOPK_MAX_K
     ("K", 101, 2),                       # K > V
     ("d", 12, 3), ("d", 4, 2), ("T", -1, 2), ("V", 0, 2),
 ])
 def test_topk_argument_errors_are_synchronous(lib, field, value, code):
-    p = kdkl.kd_topk_problem(10, 16, 100, 4, 0)
+    # V = 1000 unless the case is K > V
+    p = kdkl.kd_topk_problem(10, 16, 100 if (field, value) == ("K", 101) else 1000, 4, 0)
     setattr(p, field, value)
     assert _topk(lib, p) == code
     assert lib.kd_lmhead_topk_workspace_size(ctypes.byref(p)) == 0

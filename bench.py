@@ -460,16 +460,19 @@ def run_kdkl(args):
     if rank == 0:
         pk, pk_src = peaks()
         tokens = T * world * args.steps
-        flops_step = 8.0 * T * V * d  # 4 GEMM-equivalents per step and GPU
+        # Masked tokens are compacted away before any GEMM, so the work done is
+        # that of the counted tokens: 4 GEMM-equivalents of 2 N V d each.
+        n_counted = int(x["mask"].sum())
+        flops_step = 8.0 * n_counted * V * d
         tflops = flops_step * args.steps / (elapsed_ms / 1e3) / 1e12
-        # dominant kernel by device time; algorithmic flops per launch = 2 T V d
+        # dominant kernel by device time; algorithmic flops per launch = 2 N V d
         # per step for each of the four GEMM kinds, split over its launches
         rows = {n: (c, ms) for n, c, ms in per_kernel}
         dom = max(rows, key=lambda n: rows[n][1])
         run_name = wname  # traffic is recorded for the plain workloads only
         dom_launches, dom_ms = rows[dom]
         if dom in GEMM_KERNELS:
-            per_launch_flops = 2.0 * T * V * d * args.steps / dom_launches
+            per_launch_flops = 2.0 * n_counted * V * d * args.steps / dom_launches
             achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
             peak = pk["bf16_tflops_sustained"]
             roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
@@ -502,6 +505,8 @@ def run_kdkl(args):
             "mixed soft + hard-label distillation loss fwd+bwd tokens/s",
             "value": round(tokens / (elapsed_ms / 1e3), 1),
             "unit": "tokens/s",
+            "value_counts": "every token of the batch, masked ones included",
+            "counted_tokens_per_s": round(n_counted * world * args.steps / (elapsed_ms / 1e3), 1),
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
@@ -515,7 +520,8 @@ def run_kdkl(args):
             "data": "synthetic (seeded; bf16 H~N(0,1), W~N(0,1/d); teacher top-%d %s)" % (
                 K, "half from the student's own top-%d" % K if w.teacher == "half_overlap"
                 else "uniform distinct ids"),
-            "config": {"workload": wname, "T": T, "d": d, "V": V, "K": K, "chunk": w.chunk,
+            "config": {"workload": wname, "T": T, "counted_tokens": n_counted, "d": d, "V": V,
+                       "K": K, "chunk": w.chunk,
                        "tau": w.tau, "seed": args.seed, "global_batch_tokens": T * world,
                        "parallelism": "dp%d (independent batches)" % world,
                        "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},

@@ -84,16 +84,20 @@ size_t kd_kl_workspace_size(const kd_kl_problem* prob, int which);
  *   topk_logit [T, K] fp32        teacher's cached logits (-inf allowed, not all)
  *   mask       [T] uint8 or NULL  nonzero = token counts (NULL: all count)
  *   loss       [1] fp32 out       sum_t m[t] KL[t] / N (0 when N = 0)
- *   lse        [T] fp32 out       log sum_v exp(z[t,v]/tau), every row
- *   token_kl   [T] fp32 out or NULL   KL[t] before masking
+ *   lse        [T] fp32 out       log sum_v exp(z[t,v]/tau) of every counted token
+ *   token_kl   [T] fp32 out or NULL   KL[t] of every counted token
  * The logits z are produced tile by tile inside the SMs and never written to
- * memory. */
+ * memory. With a mask, the counted tokens are compacted first (in order) and
+ * every later step runs on them alone: a masked token costs no tensor-core
+ * work, and its lse and token_kl read 0 (they are not computed). With a NULL
+ * mask every token counts. */
 kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                         const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
                         float* loss, float* lse, float* token_kl,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* Backward: gradients of g * loss.
+/* Backward: gradients of g * loss. Masked tokens are skipped as in the
+ * forward (their dH rows are exact zeros).
  *   lse        [T] fp32           from kd_kl_forward on the same inputs
  *   grad_loss  g                  upstream dL_outer/dloss (host scalar)
  *   dH         [T, d] bf16 out    overwritten; fp32 accumulation inside, masked rows = 0
@@ -124,10 +128,11 @@ typedef struct {
 } kd_kl_options;
 
 /* Workspace: kd_kl_workspace_size(prob, 2) for the forward, (prob, 3) for the backward.
- *   lse        [T] fp32 out   logsumexp of z / tau
+ *   lse        [T] fp32 out   logsumexp of z / tau (counted tokens; masked ones read 0)
  *   lse1       [T] fp32 out   logsumexp of z (temperature 1; equals lse when tau == 1)
- *   token_loss [T] fp32 out or NULL   alpha c KL_t + (1 - alpha) CE_t before masking
- * A label outside [0, V) is reported as KD_ERR_INDEX_RANGE by kd_kl_check_status. */
+ *   token_loss [T] fp32 out or NULL   alpha c KL_t + (1 - alpha) CE_t (counted tokens)
+ * A counted token's label outside [0, V) is reported as KD_ERR_INDEX_RANGE by
+ * kd_kl_check_status (masked tokens' labels and teacher ids are not read). */
 kd_status kd_kl_forward_ex(const kd_kl_problem* prob, const kd_kl_options* opts,
                            const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
                            const float* topk_logit, const uint8_t* mask, float* loss, float* lse,

@@ -195,10 +195,33 @@ bool static_schedule() {
   return v && v[0] == '1';
 }
 
+// The prepared teacher side of a call, at the same place in the forward and
+// the backward workspaces (from `base` on), so that a backward can read the
+// forward's: sorted ids and p [T, K]; when a mask is given, the compaction of
+// the counted tokens: rowmap [T] (row -> token), invmap [T] (token -> row or
+// -1) and Hc, H's counted rows [T_pad, d] bf16 (T_pad = T rounded up to 256).
+struct TeacherLayout {
+  size_t off_sidx, off_sp, off_rowmap, off_invmap, off_Hc, end;
+};
+
+TeacherLayout teacher_layout(size_t base, const kd_kl_problem& p) {
+  TeacherLayout L{};
+  const size_t TK = (size_t)p.T * p.K;
+  size_t o = base;
+  L.off_sidx = o; o = align256(o + TK * 4);
+  L.off_sp = o; o = align256(o + TK * 4);
+  L.off_rowmap = o; o = align256(o + (size_t)p.T * 4);
+  L.off_invmap = o; o = align256(o + (size_t)p.T * 4);
+  L.off_Hc = o; o = align256(o + (size_t)round_up(p.T, 2 * BM) * p.d * 2);
+  L.end = o;
+  return L;
+}
+
 struct FwdPlan {
   bool pair;
   int m_tiles, n_tiles, nsplit, group_m, grid;
-  size_t off_sidx, off_sp, off_ent, off_pm, off_ps, off_pd, off_ps1, off_pzl, off_bsum, total;
+  TeacherLayout tl;
+  size_t off_ent, off_pm, off_ps, off_pd, off_ps1, off_pzl, off_bsum, total;
 };
 
 // Per-launch unit counters live in the workspace header (ints from this
@@ -212,8 +235,11 @@ struct BwdPlan {
   int64_t Tb_pad, Vb_pad;
   int64_t n_tblocks, n_vblocks;
   // off_ctr: one unit counter per GEMM launch (3 per block), right after the
-  // header, zeroed with it at the start of every call
-  size_t off_ctr, off_sidx, off_sp, off_G, off_dH, total;
+  // header, zeroed with it at the start of every call; tl: the teacher side
+  // (none when the backward reads the forward's)
+  size_t off_ctr;
+  TeacherLayout tl;
+  size_t off_G, off_dH, total;
 };
 
 bool problem_ok(const kd_kl_problem* p) {
@@ -238,10 +264,8 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, 
   f.nsplit = p.T > 0 ? lp.nsplit : 1;
   f.group_m = lp.group_m;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
-  size_t o = kHeaderBytes;
-  const size_t TK = (size_t)p.T * p.K;
-  f.off_sidx = o; o = align256(o + TK * 4);
-  f.off_sp = o; o = align256(o + TK * 4);
+  f.tl = teacher_layout(kHeaderBytes, p);
+  size_t o = f.tl.end;
   f.off_ent = o; o = align256(o + (size_t)p.T * 4);
   f.off_pm = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
   f.off_ps = o; o = align256(o + (size_t)f.nsplit * p.T * 4);
@@ -279,9 +303,8 @@ BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
   b.Vb_pad = round_up(b.Vb, LOGIT_BN);
   size_t o = kHeaderBytes;
   b.off_ctr = o; o = align256(o + (size_t)3 * b.n_tblocks * b.n_vblocks * 4);
-  const size_t TK = own_teacher ? (size_t)p.T * p.K : 0;
-  b.off_sidx = o; o = align256(o + TK * 4);
-  b.off_sp = o; o = align256(o + TK * 4);
+  b.tl = teacher_layout(o, p);
+  if (own_teacher) o = b.tl.end;
   b.off_G = o; o = align256(o + (size_t)b.Tb_pad * b.Vb_pad * 2);
   b.off_dH = o; o = align256(o + (size_t)p.T * p.d * 4);
   b.total = o;
@@ -413,6 +436,7 @@ struct FwdRecord {
   int32_t K;
   float temperature;
   size_t bytes;
+  const void* mask;  // the forward's mask pointer (its compaction is reused)
 };
 constexpr size_t kMaxFwdRecords = 64;
 std::mutex g_fwd_mu;
@@ -427,7 +451,7 @@ void forget_forward(const void* ws) {
     }
 }
 
-void remember_forward(const void* ws, const kd_kl_problem& p, size_t bytes) {
+void remember_forward(const void* ws, const kd_kl_problem& p, size_t bytes, const void* mask) {
   std::lock_guard<std::mutex> lk(g_fwd_mu);
   for (size_t i = 0; i < g_fwd_records.size(); ++i)
     if (g_fwd_records[i].ws == ws) {
@@ -435,17 +459,18 @@ void remember_forward(const void* ws, const kd_kl_problem& p, size_t bytes) {
       break;
     }
   if (g_fwd_records.size() >= kMaxFwdRecords) g_fwd_records.erase(g_fwd_records.begin());
-  g_fwd_records.push_back(FwdRecord{ws, p.T, p.d, p.V, p.K, p.temperature, bytes});
+  g_fwd_records.push_back(FwdRecord{ws, p.T, p.d, p.V, p.K, p.temperature, bytes, mask});
 }
 
 // True when `ws` was last filled by a forward call on the same problem (chunk
-// aside: it does not change the teacher cache) and is at least `bytes` long.
-bool forward_matches(const void* ws, size_t ws_bytes, const kd_kl_problem& p) {
+// aside: it does not change the teacher cache) with the same mask pointer,
+// and the caller says it is at least as long as that call needed.
+bool forward_matches(const void* ws, size_t ws_bytes, const kd_kl_problem& p, const void* mask) {
   std::lock_guard<std::mutex> lk(g_fwd_mu);
   for (const FwdRecord& r : g_fwd_records)
     if (r.ws == ws)
       return r.T == p.T && r.d == p.d && r.V == p.V && r.K == p.K &&
-             r.temperature == p.temperature && ws_bytes >= r.bytes;
+             r.temperature == p.temperature && ws_bytes >= r.bytes && r.mask == mask;
   return false;
 }
 
@@ -561,22 +586,33 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
   KD_CUDA(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
   if (p.T == 0) {
     KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
-    remember_forward(workspace, p, f.off_sp);
+    remember_forward(workspace, p, f.tl.end, mask);
     return KD_OK;
   }
   const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
   const float inv_tau = 1.0f / p.temperature;
   const float cl2 = 1.4426950408889634f * inv_tau;
-  int32_t* sidx = at<int32_t>(workspace, f.off_sidx);
-  float* sp = at<float>(workspace, f.off_sp);
+  int32_t* sidx = at<int32_t>(workspace, f.tl.off_sidx);
+  float* sp = at<float>(workspace, f.tl.off_sp);
   float* ent = at<float>(workspace, f.off_ent);
-
-  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
-                              inv_tau, sidx, sp, ent, n_count, status, stream));
+  // With a mask, the counted tokens are compacted first and every step
+  // after that runs on them only: masked tokens cost no tensor-core work.
+  const bool compact = mask != nullptr;
+  int* rowmap = compact ? at<int>(workspace, f.tl.off_rowmap) : nullptr;
+  int* invmap = compact ? at<int>(workspace, f.tl.off_invmap) : nullptr;
+  uint16_t* Hc = at<uint16_t>(workspace, f.tl.off_Hc);
+  const int64_t T_pad = round_up(T, 2 * BM);
+  if (compact) {
+    KD_CUDA(launch_mask_scan(mask, T, rowmap, invmap, n_count, stream));
+    KD_CUDA(launch_gather_rows(H, d, rowmap, n_count, T_pad, 2 * BM, Hc, di.num_sms, stream));
+  }
+  KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, rowmap, T,
+                              K, V, inv_tau, sidx, sp, ent, n_count, status, stream));
 
   CUtensorMap tmH, tmW;
   const int b_rows = f.pair ? LOGIT_BN / 2 : LOGIT_BN;  // W rows one CTA loads per tile
-  if (!encode_bf16_2d(&tmH, H, d, T, d, BK, BM) || !encode_bf16_2d(&tmW, W, d, V, d, BK, b_rows))
+  if (!encode_bf16_2d(&tmH, compact ? Hc : H, d, compact ? T_pad : T, d, BK, BM) ||
+      !encode_bf16_2d(&tmW, W, d, V, d, BK, b_rows))
     return KD_ERR_CUDA;
   GemmShape sh{};
   sh.inject_stall = inject_stall_from_env();
@@ -587,7 +623,14 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
   sh.units = f.m_tiles * f.nsplit;
   sh.k_blocks = (int)ceil_div(d, BK);
   sh.counter = static_schedule() ? nullptr : status + kHeaderCounter0;
+  if (compact) {
+    sh.dyn_rows = n_count;
+    sh.dyn_base = 0;
+    sh.dyn_cap = T;
+    sh.dyn_dim = 0;
+  }
   EpiParams ep{};
+  ep.rowmap = rowmap;
   ep.sidx = sidx;
   ep.sp = sp;
   ep.K = K;
@@ -613,15 +656,17 @@ static kd_status forward_impl(const kd_kl_problem* prob, const kd_kl_options* op
   double* bsum = at<double>(workspace, f.off_bsum);
   if (mix) {
     const MixWeights mw = mix_weights(p, *opts);
-    KD_CUDA(launch_lse_combine_mix(ep.pm, ep.ps, ep.pd, ep.ps1, ep.pzl, f.nsplit, T, ent, mask, cl2,
-                                   inv_tau, mw.kl, mw.ce, lse, lse1, token_kl, bsum, stream));
+    KD_CUDA(launch_lse_combine_mix(ep.pm, ep.ps, ep.pd, ep.ps1, ep.pzl, f.nsplit, T, ent, mask,
+                                   invmap, cl2, inv_tau, mw.kl, mw.ce, lse, lse1, token_kl, bsum,
+                                   stream));
   } else {
-    KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, cl2, inv_tau, lse,
-                               token_kl, bsum, stream));
+    KD_CUDA(launch_lse_combine(ep.pm, ep.ps, ep.pd, f.nsplit, T, ent, mask, invmap, cl2, inv_tau,
+                               lse, token_kl, bsum, stream));
   }
   KD_CUDA(launch_loss_finalize(bsum, combine_blocks(T), n_count, loss, stream));
-  // the teacher region (header, sorted ids, their p) is what a backward reuses
-  remember_forward(workspace, p, f.off_sp + (size_t)p.T * p.K * 4);
+  // the teacher side (header with N, sorted ids and p, the compaction) is
+  // what a backward reuses
+  remember_forward(workspace, p, f.tl.end, mask);
   return KD_OK;
 }
 
@@ -656,7 +701,7 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   kd_status st = validate_common(prob, H, W, reuse ? fwd_ws : topk_idx,
                                  reuse ? fwd_ws : topk_logit, workspace);
   if (st != KD_OK) return st;
-  if (reuse && !forward_matches(fwd_ws, fwd_ws_bytes, *prob)) return KD_ERR_INVALID_ARG;
+  if (reuse && !forward_matches(fwd_ws, fwd_ws_bytes, *prob, mask)) return KD_ERR_INVALID_ARG;
   const bool mix = opts != nullptr;
   if (mix && ((st = validate_options(prob, opts)) != KD_OK)) return st;
   // temperature-1 logsumexp: needed when the CE term is on and tau != 1
@@ -677,7 +722,7 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   int* status = at<int>(workspace, 0);
   // the counted-token total N: this call's own, or the forward's
   int* n_count = reuse ? const_cast<int*>(static_cast<const int*>(fwd_ws)) + 1 : status + 1;
-  KD_CUDA(cudaMemsetAsync(workspace, 0, b.off_sidx, stream));  // header and unit counters
+  KD_CUDA(cudaMemsetAsync(workspace, 0, b.tl.off_sidx, stream));  // header and unit counters
   int* counters = static_schedule() ? nullptr : at<int>(workspace, b.off_ctr);
   int launch_no = 0;  // index of the next GEMM launch's counter
   auto next_counter = [&]() { return counters ? counters + launch_no++ : nullptr; };
@@ -688,27 +733,42 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   const int T = (int)p.T, K = p.K, V = (int)p.V, d = (int)p.d;
   const float inv_tau = 1.0f / p.temperature;
   const float cl2 = 1.4426950408889634f * inv_tau;
-  // Sorted teacher ids and probabilities: the forward workspace's (right
-  // after its header), or prepared here.
-  void* fws = const_cast<void*>(fwd_ws);
-  int32_t* sidx = reuse ? at<int32_t>(fws, kHeaderBytes) : at<int32_t>(workspace, b.off_sidx);
-  float* sp = reuse ? at<float>(fws, kHeaderBytes + align256((size_t)p.T * p.K * 4))
-                    : at<float>(workspace, b.off_sp);
+  // The teacher side (sorted ids and p; with a mask, the compaction of the
+  // counted tokens): the forward workspace's, at the same offsets, or
+  // prepared here.
+  char* tws = reuse ? static_cast<char*>(const_cast<void*>(fwd_ws)) : static_cast<char*>(workspace);
+  const TeacherLayout tl = reuse ? teacher_layout(kHeaderBytes, p) : b.tl;
+  int32_t* sidx = at<int32_t>(tws, tl.off_sidx);
+  float* sp = at<float>(tws, tl.off_sp);
+  const bool compact = mask != nullptr;
+  int* rowmap = compact ? at<int>(tws, tl.off_rowmap) : nullptr;
+  int* invmap = compact ? at<int>(tws, tl.off_invmap) : nullptr;
+  uint16_t* Hc = at<uint16_t>(tws, tl.off_Hc);
+  const int64_t T_pad = round_up(T, 2 * BM);
   uint16_t* Gbuf = at<uint16_t>(workspace, b.off_G);
   float* dH_acc = at<float>(workspace, b.off_dH);
 
-  if (!reuse)
-    KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, T, K, V,
-                                inv_tau, sidx, sp, nullptr, n_count, status, stream));
+  if (!reuse) {
+    if (compact) {
+      KD_CUDA(launch_mask_scan(mask, T, rowmap, invmap, n_count, stream));
+      KD_CUDA(launch_gather_rows(H, d, rowmap, n_count, T_pad, 2 * BM, Hc, di.num_sms, stream));
+    }
+    KD_CUDA(launch_teacher_prep(topk_idx, topk_logit, mask, mix ? opts->labels : nullptr, rowmap,
+                                T, K, V, inv_tau, sidx, sp, nullptr, n_count, status, stream));
+  }
 
   const bool pair = use_pair();
   const int tile_m = pair ? 2 * BM : BM;
   const int procs = gemm_procs(di.num_sms, pair);
   const int cta_per_proc = pair ? 2 : 1;
+  // Rows of the token operand: the compacted counted tokens, or H itself.
+  const uint16_t* Hop = compact ? Hc : H;
+  const int64_t H_rows = compact ? T_pad : T;
   CUtensorMap tmH_K, tmW_K, tmW_MN, tmH_MN;
-  if (!encode_bf16_2d(&tmH_K, H, d, T, d, BK, BM) ||
+  if (!encode_bf16_2d(&tmH_K, Hop, d, H_rows, d, BK, BM) ||
       !encode_bf16_2d(&tmW_K, W, d, V, d, BK, pair ? LOGIT_BN / 2 : LOGIT_BN) ||
-      !encode_bf16_2d(&tmW_MN, W, d, V, d, 64, BK) || !encode_bf16_2d(&tmH_MN, H, d, T, d, 64, BK))
+      !encode_bf16_2d(&tmW_MN, W, d, V, d, 64, BK) ||
+      !encode_bf16_2d(&tmH_MN, Hop, d, H_rows, d, 64, BK))
     return KD_ERR_CUDA;
 
   // N tile of the dH / dW GEMMs (hidden dimension). 192-wide tiles avoid the
@@ -742,7 +802,14 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         sh.a_m0 = row0;
         sh.b_n0 = col0;
         sh.counter = next_counter();
+        if (compact) {  // only the block's counted tokens
+          sh.dyn_rows = n_count;
+          sh.dyn_base = row0;
+          sh.dyn_cap = rows;
+          sh.dyn_dim = 0;
+        }
         EpiParams ep{};
+        ep.rowmap = rowmap;
         ep.sidx = sidx;
         ep.sp = sp;
         ep.K = K;
@@ -753,7 +820,7 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         ep.cols = cols;
         ep.cl2 = cl2;
         ep.lse = lse;
-        ep.mask = mask;
+        ep.mask = compact ? nullptr : mask;
         ep.n_count = n_count;
         ep.g_over_tau = grad_loss * inv_tau;
         ep.G = Gbuf;
@@ -785,6 +852,12 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         sh.k_blocks = (int)ceil_div(cols, BK);
         sh.b_k0 = col0;
         sh.counter = next_counter();
+        if (compact) {
+          sh.dyn_rows = n_count;
+          sh.dyn_base = row0;
+          sh.dyn_cap = rows;
+          sh.dyn_dim = 0;  // M: the block's counted tokens
+        }
         EpiParams ep{};
         ep.out = dH_acc + (int64_t)row0 * d;
         ep.ldo = d;
@@ -809,6 +882,12 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         sh.k_blocks = (int)ceil_div(rows, BK);
         sh.b_k0 = row0;
         sh.counter = next_counter();
+        if (compact) {
+          sh.dyn_rows = n_count;
+          sh.dyn_base = row0;
+          sh.dyn_cap = rows;
+          sh.dyn_dim = 1;  // K: the block's counted tokens
+        }
         EpiParams ep{};
         ep.out = dW + (int64_t)col0 * d;
         ep.ldo = d;
@@ -821,7 +900,8 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
       }
     }
   }
-  KD_CUDA(launch_f32_to_bf16(dH_acc, dH, (long long)p.T * p.d, di.num_sms, stream));
+  // dH rows back to the callers' tokens; masked rows are exact zeros
+  KD_CUDA(launch_f32_to_bf16(dH_acc, dH, (long long)p.T * p.d, d, invmap, di.num_sms, stream));
   return KD_OK;
 }
 

@@ -54,24 +54,37 @@ cudaError_t launch_kernel_cluster(const char* name, void (*kern)(KArgs...), dim3
 }
 
 // kernels_small.cu
+// rowmap == nullptr: row t <- token t, and the mask is counted into *n_count.
+// Else row r <- token rowmap[r] for r < *n_count (set by launch_mask_scan).
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
-                                const int32_t* labels, int T, int K, int V, float inv_tau,
-                                int32_t* sidx, float* sp, float* ent, int* n_count, int* status,
-                                cudaStream_t stream);
+                                const int32_t* labels, const int* rowmap, int T, int K, int V,
+                                float inv_tau, int32_t* sidx, float* sp, float* ent, int* n_count,
+                                int* status, cudaStream_t stream);
+// Counted-token compaction: rowmap [T], invmap [T], *n_count = N.
+cudaError_t launch_mask_scan(const uint8_t* mask, int T, int* rowmap, int* invmap, int* n_count,
+                             cudaStream_t stream);
+// Hc rows [0, N) <- H rows rowmap[0..N); rows up to N rounded up to `round`
+// (at most rows_cap) zeroed.
+cudaError_t launch_gather_rows(const uint16_t* H, int d, const int* rowmap, const int* n_count,
+                               long long rows_cap, int round, uint16_t* Hc, int num_sms,
+                               cudaStream_t stream);
 int combine_blocks(int T);
 cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
-                               const float* ent, const uint8_t* mask, float cl2, float inv_tau,
-                               float* lse, float* token_kl, double* block_sums,
-                               cudaStream_t stream);
+                               const float* ent, const uint8_t* mask, const int* invmap,
+                               float cl2, float inv_tau, float* lse, float* token_kl,
+                               double* block_sums, cudaStream_t stream);
 cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float* pd,
                                    const float* ps1, const float* pzl, int nsplit, int T,
-                                   const float* ent, const uint8_t* mask, float cl2, float inv_tau,
-                                   float kl_w, float ce_w, float* lse, float* lse1,
-                                   float* token_loss, double* block_sums, cudaStream_t stream);
+                                   const float* ent, const uint8_t* mask, const int* invmap,
+                                   float cl2, float inv_tau, float kl_w, float ce_w, float* lse,
+                                   float* lse1, float* token_loss, double* block_sums,
+                                   cudaStream_t stream);
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,
                                  float* loss, cudaStream_t stream);
-cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
-                               cudaStream_t stream);
+// out [T, d] bf16 <- in rows (invmap[t], or t when invmap is nullptr; zeros
+// for invmap[t] < 0); n = T * d.
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int d,
+                               const int* invmap, int num_sms, cudaStream_t stream);
 // merge of per-split top-K lists; shared memory = topk_merge_p2() * 8 bytes
 int topk_merge_p2(int nsplit, int K);
 cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, const int* unit_cnt,

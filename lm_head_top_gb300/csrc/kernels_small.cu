@@ -75,13 +75,16 @@ __device__ __forceinline__ float row_max(float v) {
   return v;
 }
 
+// rowmap == nullptr: output row t is token t, and the kernel counts the mask
+// into *n_count. Otherwise output row r (r < *n_count, set by the mask scan)
+// is token rowmap[r], and rows from *n_count on are left unwritten.
 template <int L, int E, bool WIDE>
 __global__ void __launch_bounds__(PREP_THREADS)
     teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ logit,
                         const uint8_t* __restrict__ mask, const int32_t* __restrict__ labels,
-                        int T, int K, int V, float inv_tau, int vec_io, int32_t* __restrict__ sidx,
-                        float* __restrict__ sp, float* __restrict__ ent, int* n_count,
-                        int* status) {
+                        const int* __restrict__ rowmap, int T, int K, int V, float inv_tau,
+                        int vec_io, int32_t* __restrict__ sidx, float* __restrict__ sp,
+                        float* __restrict__ ent, int* n_count, int* status) {
   using Key = typename PrepKey<WIDE>::T;
   constexpr int N = L * E;
   constexpr int LOGN = Log2<N>::value;
@@ -91,15 +94,17 @@ __global__ void __launch_bounds__(PREP_THREADS)
   const int lane = threadIdx.x & 31;
   const int row = threadIdx.x / L;  // row slot in the block
   const int l = threadIdx.x % L;    // lane within the row
-  const int t = blockIdx.x * ROWS + row;
-  const bool live = t < T;
+  const int t = blockIdx.x * ROWS + row;  // output row
+  const bool live = t < (rowmap ? *n_count : T);
+  const int src = live ? (rowmap ? __ldg(rowmap + t) : t) : 0;  // token read
   if (threadIdx.x == 0) block_count = 0;
   __syncthreads();
 
   // ---- one read of the row into registers
   int id[E];
   float a[E];
-  const long long base = (long long)(live ? t : 0) * K;
+  const long long base = (long long)src * K;
+  const long long obase = (long long)t * K;
   // 16-byte loads and stores when rows and pointers allow (host-checked)
   const bool vec4 = (E % 4 == 0) && vec_io != 0;
   if (vec4) {
@@ -208,8 +213,8 @@ __global__ void __launch_bounds__(PREP_THREADS)
 
   // ---- write the sorted (id, p) row
   if (live) {
-    int32_t* so = sidx + base;
-    float* po = sp + base;
+    int32_t* so = sidx + obase;
+    float* po = sp + obase;
     int oid[E];
     float op[E];
 #pragma unroll
@@ -238,10 +243,11 @@ __global__ void __launch_bounds__(PREP_THREADS)
       }
     }
     if (l == 0) {
-      if (labels && (labels[t] < 0 || labels[t] >= V)) record_error(status, DEV_ERR_INDEX_RANGE);
+      if (labels && (labels[src] < 0 || labels[src] >= V)) record_error(status, DEV_ERR_INDEX_RANGE);
       if (ent) ent[t] = h;
     }
   }
+  if (rowmap) return;  // N came from the mask scan
   const bool counted = live && l == 0 && (mask == nullptr || mask[t] != 0);
   const uint32_t cnt = __popc(__ballot_sync(0xffffffffu, counted));
   if (lane == 0 && cnt) atomicAdd(&block_count, (int)cnt);
@@ -254,25 +260,32 @@ constexpr int COMBINE_THREADS = 256;
 __global__ void __launch_bounds__(COMBINE_THREADS)
     lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                        const float* __restrict__ pd, int nsplit, int T,
-                       const float* __restrict__ ent, const uint8_t* __restrict__ mask, float cl2,
-                       float inv_tau, float* __restrict__ lse, float* __restrict__ token_kl,
+                       const float* __restrict__ ent, const uint8_t* __restrict__ mask,
+                       const int* __restrict__ invmap, float cl2, float inv_tau,
+                       float* __restrict__ lse, float* __restrict__ token_kl,
                        double* __restrict__ block_sums) {
+  // invmap: token t's row among the partials (-1: masked, never computed:
+  // lse and KL read 0), or nullptr (row t).
   const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
   double contrib = 0.0;
   if (t < T) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + t]);
-    float S = 0.f, D = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const long long o = (long long)s * T + t;
-      S += ps[o] * exp2f((pm[o] - M) * cl2);
-      D += pd[o];
+    const int r = invmap ? invmap[t] : t;
+    float l = 0.f, kl = 0.f;
+    if (r >= 0) {
+      float M = -INFINITY;
+      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + r]);
+      float S = 0.f, D = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const long long o = (long long)s * T + r;
+        S += ps[o] * exp2f((pm[o] - M) * cl2);
+        D += pd[o];
+      }
+      l = M * inv_tau + logf(S);
+      kl = ent[r] - D * inv_tau + l;
     }
-    const float l = M * inv_tau + logf(S);
-    const float kl = ent[t] - D * inv_tau + l;
     lse[t] = l;
     if (token_kl) token_kl[t] = kl;
-    if (mask == nullptr || mask[t] != 0) contrib = (double)kl;
+    if (invmap ? r >= 0 : (mask == nullptr || mask[t] != 0)) contrib = (double)kl;
   }
   // fixed-shape tree reduction: deterministic
   __shared__ double red[COMBINE_THREADS];
@@ -291,30 +304,34 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
                            const float* __restrict__ pd, const float* __restrict__ ps1,
                            const float* __restrict__ pzl, int nsplit, int T,
                            const float* __restrict__ ent, const uint8_t* __restrict__ mask,
-                           float cl2, float inv_tau, float kl_w, float ce_w,
-                           float* __restrict__ lse, float* __restrict__ lse1,
+                           const int* __restrict__ invmap, float cl2, float inv_tau, float kl_w,
+                           float ce_w, float* __restrict__ lse, float* __restrict__ lse1,
                            float* __restrict__ token_loss, double* __restrict__ block_sums) {
   const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
   double contrib = 0.0;
   if (t < T) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + t]);
-    float S = 0.f, S1 = 0.f, D = 0.f, Z = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const long long o = (long long)s * T + t;
-      S += ps[o] * exp2f((pm[o] - M) * cl2);
-      S1 += ps1[o] * exp2f((pm[o] - M) * 1.4426950408889634f);
-      D += pd[o];
-      Z += pzl[o];
+    const int r = invmap ? invmap[t] : t;
+    float l = 0.f, l1 = 0.f, tok = 0.f;
+    if (r >= 0) {
+      float M = -INFINITY;
+      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + r]);
+      float S = 0.f, S1 = 0.f, D = 0.f, Z = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const long long o = (long long)s * T + r;
+        S += ps[o] * exp2f((pm[o] - M) * cl2);
+        S1 += ps1[o] * exp2f((pm[o] - M) * 1.4426950408889634f);
+        D += pd[o];
+        Z += pzl[o];
+      }
+      l = M * inv_tau + logf(S);
+      l1 = M + logf(S1);
+      const float kl = ent[r] - D * inv_tau + l;
+      tok = kl_w * kl + ce_w * (l1 - Z);
     }
-    const float l = M * inv_tau + logf(S);
-    const float l1 = M + logf(S1);
-    const float kl = ent[t] - D * inv_tau + l;
-    const float tok = kl_w * kl + ce_w * (l1 - Z);
     lse[t] = l;
     lse1[t] = l1;
     if (token_loss) token_loss[t] = tok;
-    if (mask == nullptr || mask[t] != 0) contrib = (double)tok;
+    if (invmap ? r >= 0 : (mask == nullptr || mask[t] != 0)) contrib = (double)tok;
   }
   __shared__ double red[COMBINE_THREADS];
   red[threadIdx.x] = contrib;
@@ -344,12 +361,105 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
-                                   long long n4) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float4 v = in[i];
-    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+// out row t = bf16(in row invmap[t]), or zeros when invmap[t] < 0; invmap
+// nullptr: row t. One block per row at a time, d4 = d / 4 float4 per row.
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, int T,
+                                   int d4, const int* __restrict__ invmap) {
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const int r = invmap ? __ldg(invmap + t) : t;
+    uint2* o = out + (long long)t * d4;
+    if (r < 0) {
+      for (int c = threadIdx.x; c < d4; c += blockDim.x) o[c] = make_uint2(0u, 0u);
+      continue;
+    }
+    const float4* src = in + (long long)r * d4;
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 v = src[c];
+      o[c] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+  }
+}
+
+// Compaction of the counted tokens, one block: rowmap[r] = the r-th token
+// with mask != 0 (in order), invmap[t] = its r or -1, *n_count = N. The mask
+// is taken in tiles of 32 x 1024 tokens: warp w owns 32 consecutive 32-token
+// chunks of a tile, counts them with ballots (lane j keeps chunk j's count),
+// a block scan gives each chunk its first row, and a second pass writes the
+// maps. Loads and invmap stores are coalesced 32-token pieces.
+constexpr int SCAN_THREADS = 1024;
+__global__ void __launch_bounds__(SCAN_THREADS)
+    mask_scan_kernel(const uint8_t* __restrict__ mask, int T, int* __restrict__ rowmap,
+                     int* __restrict__ invmap, int* __restrict__ n_count) {
+  __shared__ int warp_base[SCAN_THREADS / 32];
+  __shared__ int tile_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t below = (1u << lane) - 1u;
+  constexpr long long TILE = 32LL * SCAN_THREADS;  // tokens per tile
+  int base = 0;                                     // rows before this tile
+  for (long long t0 = 0; t0 < T; t0 += TILE) {
+    const long long w0 = t0 + (long long)warp * 32 * 32;  // this warp's first token
+    int my_count = 0;                                     // chunk `lane` of this warp
+    for (int j = 0; j < 32; ++j) {
+      const long long t = w0 + (long long)j * 32 + lane;
+      const bool on = t < T && mask[t] != 0;
+      const int c = __popc(__ballot_sync(0xffffffffu, on));
+      if (lane == j) my_count = c;
+    }
+    int incl = my_count;  // chunks of this warp, in order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_base[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int wt = warp_base[lane];
+      int wi = wt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      warp_base[lane] = wi - wt;
+      if (lane == 31) tile_total = wi;
+    }
+    __syncthreads();
+    const int chunk_first = base + warp_base[warp] + incl - my_count;  // chunk `lane`'s first row
+    for (int j = 0; j < 32; ++j) {
+      const long long t = w0 + (long long)j * 32 + lane;
+      const bool on = t < T && mask[t] != 0;
+      const uint32_t b = __ballot_sync(0xffffffffu, on);
+      const int first = __shfl_sync(0xffffffffu, chunk_first, j);
+      if (t < T) {
+        const int r = first + __popc(b & below);
+        if (on) rowmap[r] = (int)t;
+        invmap[t] = on ? r : -1;
+      }
+    }
+    base += tile_total;
+    __syncthreads();  // warp_base and tile_total are rewritten by the next tile
+  }
+  if (threadIdx.x == 0) *n_count = base;
+}
+
+// Hc row r = H row rowmap[r] for r < N; rows N .. (N rounded up to `round`)
+// are zeroed (the partial last tile the GEMMs read). One block per row at a
+// time, 16-byte pieces.
+__global__ void gather_rows_kernel(const uint4* __restrict__ H, int row16,
+                                   const int* __restrict__ rowmap, const int* __restrict__ n_count,
+                                   long long rows_cap, int round, uint4* __restrict__ Hc) {
+  const long long N = *n_count;
+  long long end = (N + round - 1) / round * round;
+  if (end > rows_cap) end = rows_cap;
+  for (long long r = blockIdx.x; r < end; r += gridDim.x) {
+    uint4* o = Hc + r * row16;
+    if (r >= N) {
+      for (int c = threadIdx.x; c < row16; c += blockDim.x) o[c] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const uint4* src = H + (long long)__ldg(rowmap + r) * row16;
+    for (int c = threadIdx.x; c < row16; c += blockDim.x) o[c] = src[c];
   }
 }
 
@@ -534,26 +644,26 @@ namespace {
 
 template <int L, int E>
 cudaError_t launch_prep(bool wide, const int32_t* idx, const float* logit, const uint8_t* mask,
-                        const int32_t* labels, int T, int K, int V, float inv_tau, int vec_io,
-                        int32_t* sidx,
+                        const int32_t* labels, const int* rowmap, int T, int K, int V,
+                        float inv_tau, int vec_io, int32_t* sidx,
                         float* sp, float* ent, int* n_count, int* status, cudaStream_t stream) {
   constexpr int rows = PREP_THREADS / L;
   const dim3 grid((T + rows - 1) / rows);
   if (wide)
     return launch_kernel("teacher_prep", teacher_prep_kernel<L, E, true>, grid, dim3(PREP_THREADS),
-                         0, stream, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp,
-                         ent, n_count, status);
+                         0, stream, idx, logit, mask, labels, rowmap, T, K, V, inv_tau, vec_io,
+                         sidx, sp, ent, n_count, status);
   return launch_kernel("teacher_prep", teacher_prep_kernel<L, E, false>, grid, dim3(PREP_THREADS),
-                       0, stream, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp,
-                       ent, n_count, status);
+                       0, stream, idx, logit, mask, labels, rowmap, T, K, V, inv_tau, vec_io,
+                       sidx, sp, ent, n_count, status);
 }
 
 }  // namespace
 
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
-                                const int32_t* labels, int T, int K, int V, float inv_tau,
-                                int32_t* sidx, float* sp, float* ent, int* n_count, int* status,
-                                cudaStream_t stream) {
+                                const int32_t* labels, const int* rowmap, int T, int K, int V,
+                                float inv_tau, int32_t* sidx, float* sp, float* ent, int* n_count,
+                                int* status, cudaStream_t stream) {
   // Rows of up to 128 entries take 16 lanes (two rows per warp), longer rows
   // a whole warp. Packed 32-bit keys when every id fits beside the position.
   int n = 16;
@@ -565,8 +675,8 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
   auto a16 = [](const void* q) { return ((uintptr_t)q & 15u) == 0; };
   const int vec_io = (K % 4 == 0 && a16(idx) && a16(logit) && a16(sidx) && a16(sp)) ? 1 : 0;
 #define KDKL_PREP(L, E)                                                                     \
-  launch_prep<L, E>(wide, idx, logit, mask, labels, T, K, V, inv_tau, vec_io, sidx, sp, ent,  \
-                    n_count, status, stream)
+  launch_prep<L, E>(wide, idx, logit, mask, labels, rowmap, T, K, V, inv_tau, vec_io, sidx,   \
+                    sp, ent, n_count, status, stream)
   if (K <= 16) return KDKL_PREP(16, 1);
   if (K <= 32) return KDKL_PREP(16, 2);
   if (K <= 64) return KDKL_PREP(16, 4);
@@ -579,22 +689,23 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
 int combine_blocks(int T) { return (T + COMBINE_THREADS - 1) / COMBINE_THREADS; }
 
 cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
-                               const float* ent, const uint8_t* mask, float cl2, float inv_tau,
-                               float* lse, float* token_kl, double* block_sums,
-                               cudaStream_t stream) {
+                               const float* ent, const uint8_t* mask, const int* invmap,
+                               float cl2, float inv_tau, float* lse, float* token_kl,
+                               double* block_sums, cudaStream_t stream) {
   return launch_kernel("lse_combine", lse_combine_kernel, dim3(combine_blocks(T)),
-                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nsplit, T, ent, mask, cl2,
-                       inv_tau, lse, token_kl, block_sums);
+                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nsplit, T, ent, mask, invmap,
+                       cl2, inv_tau, lse, token_kl, block_sums);
 }
 
 cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float* pd,
                                    const float* ps1, const float* pzl, int nsplit, int T,
-                                   const float* ent, const uint8_t* mask, float cl2, float inv_tau,
-                                   float kl_w, float ce_w, float* lse, float* lse1,
-                                   float* token_loss, double* block_sums, cudaStream_t stream) {
+                                   const float* ent, const uint8_t* mask, const int* invmap,
+                                   float cl2, float inv_tau, float kl_w, float ce_w, float* lse,
+                                   float* lse1, float* token_loss, double* block_sums,
+                                   cudaStream_t stream) {
   return launch_kernel("lse_combine_mix", lse_combine_mix_kernel, dim3(combine_blocks(T)),
                        dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, ps1, pzl, nsplit, T, ent,
-                       mask, cl2, inv_tau, kl_w, ce_w, lse, lse1, token_loss, block_sums);
+                       mask, invmap, cl2, inv_tau, kl_w, ce_w, lse, lse1, token_loss, block_sums);
 }
 
 cudaError_t launch_loss_finalize(const double* block_sums, int nblocks, const int* n_count,
@@ -622,16 +733,28 @@ cudaError_t launch_topk_merge(const float* unit_val, const int32_t* unit_id, con
                        unit_val, unit_id, unit_cnt, row_key, nsplit, T, K, cap, out_id, out_val);
 }
 
-cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int num_sms,
+cudaError_t launch_mask_scan(const uint8_t* mask, int T, int* rowmap, int* invmap, int* n_count,
+                             cudaStream_t stream) {
+  return launch_kernel("mask_scan", mask_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, stream, mask,
+                       T, rowmap, invmap, n_count);
+}
+
+cudaError_t launch_gather_rows(const uint16_t* H, int d, const int* rowmap, const int* n_count,
+                               long long rows_cap, int round, uint16_t* Hc, int num_sms,
                                cudaStream_t stream) {
-  const long long n4 = n / 4;  // n is a multiple of 8 (d % 8 == 0)
-  long long blocks = (n4 + 255) / 256;
-  const long long cap = (long long)num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
+  const int row16 = d / 8;  // 16-byte pieces per bf16 row (d % 8 == 0)
+  return launch_kernel("gather_rows", gather_rows_kernel, dim3((unsigned)num_sms * 8), dim3(256), 0,
+                       stream, reinterpret_cast<const uint4*>(H), row16, rowmap, n_count, rows_cap,
+                       round, reinterpret_cast<uint4*>(Hc));
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, long long n, int d,
+                               const int* invmap, int num_sms, cudaStream_t stream) {
+  const int T = (int)(n / d);  // n = T * d, d a multiple of 8
+  const int blocks = std::max(1, std::min(T, num_sms * 8));
   return launch_kernel("f32_to_bf16", f32_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0,
                        stream, reinterpret_cast<const float4*>(in), reinterpret_cast<uint2*>(out),
-                       n4);
+                       T, d / 4, invmap);
 }
 
 }  // namespace kdkl

@@ -94,6 +94,12 @@ struct GemmShape {
   // producer takes the next unit with atomicAdd. nullptr: static round-robin
   // (CTA group g takes units g, g + groups, ...), kept to compare schedules.
   int* counter;
+  // Token rows counted on the device (masked tokens compacted away): when
+  // non-null, this launch's live extent along dyn_dim (0: the M rows of A,
+  // 1: the K reduction) is clamp(*dyn_rows - dyn_base, 0, dyn_cap), and
+  // m_tiles / units or k_blocks shrink to it before any role starts.
+  const int* dyn_rows;
+  int dyn_base, dyn_cap, dyn_dim;
 };
 
 // n-tile range [nb, ne) of split s.
@@ -115,6 +121,7 @@ __device__ __forceinline__ void split_range(const GemmShape& sh, int s, int& nb,
 
 struct EpiParams {
   // EPI_LSE and EPI_GRAD
+  const int* rowmap;    // compacted row -> caller's token (lse, mask, labels), or nullptr
   const int32_t* sidx;  // [T, K] teacher ids sorted ascending per row
   const float* sp;      // [T, K] teacher probabilities in the same order
   int K;
@@ -306,7 +313,7 @@ __device__ __forceinline__ int lower_bound_row(const int32_t* row, int K, int v)
 template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmShape sh, const EpiParams ep, int* status) {
+                   const GemmShape sh_in, const EpiParams ep, int* status) {
   using Cfg = TileCfg<BN, PAIR>;
   constexpr bool IS_LSE = EPI == EPI_LSE || EPI == EPI_LSE_MIX;
   constexpr bool IS_GRAD = EPI == EPI_GRAD || EPI == EPI_GRAD_MIX;
@@ -338,6 +345,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   auto ufull_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + i); };
   auto uempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + NSLOT + i); };
+
+  // Every role shrinks the shape to the live rows the same way, so they all
+  // see the same units and K steps.
+  GemmShape sh = sh_in;
+  int live_rows = IS_LSE || IS_GRAD ? ep.rows : 0;  // rows whose token counts
+  if (sh.dyn_rows) {
+    const int a = max(0, min(*sh.dyn_rows - sh.dyn_base, sh.dyn_cap));
+    if (sh.dyn_dim == 0) {
+      sh.m_tiles = min(sh.m_tiles, (a + TILE_M - 1) / TILE_M);
+      sh.units = sh.m_tiles * sh.nsplit;
+      live_rows = min(live_rows, a);
+    } else {
+      sh.k_blocks = min(sh.k_blocks, (a + BK - 1) / BK);
+    }
+  }
+  // No K steps (no live token in a dW launch): no copies and no MMAs; the
+  // epilogue writes zeros (or adds nothing) without touching TMEM.
+  const bool no_k = sh.k_blocks == 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -520,6 +545,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (!take_unit(uq, u)) break;
         release_unit(uq);
         if (u < 0) break;
+        if (no_k) continue;  // nothing to multiply: the epilogue writes zeros
         int m, s, nb, ne;
         unit_coords(sh, u, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
@@ -646,7 +672,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int cursor = ep.K, cur_id = 0x7fffffff;
       const int32_t* id_row = nullptr;
       const float* p_row = nullptr;
-      bool row_ok = false;
+      bool row_ok = false;    // the row exists in this launch
+      bool row_live = false;  // ... and holds a token (a counted one when compacted)
       // EPI_TOPK row state: admission threshold and candidate count
       float th = INFINITY;
       int cnt = 0;
@@ -665,16 +692,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int lab = -1;
       if (IS_LSE || IS_GRAD) {
         row_ok = r < ep.rows;
-        if (row_ok) {
-          const long long tok = (long long)ep.row0 + r;
-          id_row = ep.sidx + tok * ep.K;
-          p_row = ep.sp + tok * ep.K;
+        row_live = r < live_rows;
+        if (row_live) {
+          // trow: the row of the teacher cache, partials and G; tok: the
+          // caller's token (lse, mask, labels), the same unless compacted
+          const long long trow = (long long)ep.row0 + r;
+          const long long tok = ep.rowmap ? (long long)__ldg(ep.rowmap + trow) : trow;
+          id_row = ep.sidx + trow * ep.K;
+          p_row = ep.sp + trow * ep.K;
           cursor = lower_bound_row(id_row, ep.K, ep.col0 + nb * BN);
           cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
           if (IS_GRAD) {
             lse2 = __ldg(ep.lse + tok) * 1.4426950408889634f;
             const int n = *ep.n_count;
-            const bool counted = ep.mask == nullptr || __ldg(ep.mask + tok) != 0;
+            const bool counted =
+                ep.rowmap || ep.mask == nullptr || __ldg(ep.mask + tok) != 0;
             scale = (counted && n > 0) ? ep.g_over_tau / (float)n : 0.f;
             if (MIX) {
               lse12 = __ldg(ep.lse1 + tok) * 1.4426950408889634f;
@@ -713,7 +745,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         }
-        bool got = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status, limit);
+        bool got = no_k || mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status, limit);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
           ok = false;
@@ -747,7 +779,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           float v[32];
           __syncwarp();
-          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          if (no_k) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          } else {
+            tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          }
           if (IS_LSE) {
             const int vid0 = ep.col0 + cl;
             if (cl + 32 > ep.cols) {
@@ -773,9 +810,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               run_s1 = fmaf(run_s1, ex2_approx((run_max - nm) * L2E), acc1);
             }
             run_max = nm;
-            if (MIX && row_ok && lab >= vid0 && lab < vid0 + 32 && lab < ep.col0 + ep.cols)
+            if (MIX && row_live && lab >= vid0 && lab < vid0 + 32 && lab < ep.col0 + ep.cols)
               zl = select32(v, lab - vid0);
-            if (row_ok) {
+            if (row_live) {
               const int vend = ep.col0 + min(cl + 32, ep.cols);
               while (cur_id < vend) {
                 if (cur_id >= vid0) dot = fmaf(__ldg(p_row + cursor), select32(v, cur_id - vid0), dot);
@@ -795,7 +832,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const float q1 = ep.same_tau ? qt : ex2_approx(fmaf(v[j], L2E, -lse12));
                 g[j] = fmaf(qt, w_kl, q1 * w_ce);
               }
-              if (row_ok && lab >= vid0 && lab < vid0 + 32) {
+              if (row_live && lab >= vid0 && lab < vid0 + 32) {
                 const int jl = lab - vid0;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) g[j] = (j == jl) ? g[j] - w_ce : g[j];
@@ -805,6 +842,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < 32; ++j) g[j] = ex2_approx(fmaf(v[j], ep.cl2, -lse2));
             }
             if (row_ok) {
+              // rows past the live ones (compacted tokens end mid-tile) get
+              // zeros: their teacher rows are never read (cursor stays at K)
               const int vend = ep.col0 + min(cl + 32, ep.cols);
               while (cur_id < vend) {
                 if (cur_id >= vid0) {
@@ -816,7 +855,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ++cursor;
                 cur_id = cursor < ep.K ? __ldg(id_row + cursor) : 0x7fffffff;
               }
-              if (MIX) scale = 1.f;  // weights already applied
+              if (MIX) scale = row_live ? 1.f : 0.f;  // weights already applied
+              if (!row_live) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = 0.f;
+              }
               uint4* dst = reinterpret_cast<uint4*>(ep.G + (long long)r * ep.ldg + cl);
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -860,6 +903,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
+        if (no_k) continue;  // no accumulator was used
         if (lane == 0) {
           if (PAIR)
             mbar_arrive_cluster(tempty_remote0 + 8u * acc);  // the leader's barrier
@@ -886,7 +930,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         pend_r0 = m * TILE_M + (int)rank * BM + q * 32;
         bank ^= 1;
       }
-      if (IS_LSE && row_ok) {
+      if (IS_LSE && row_live) {
         const long long o = (long long)s * ep.T + ep.row0 + r;
         ep.pm[o] = run_max;
         ep.ps[o] = run_sum;

@@ -114,7 +114,9 @@ def test_workspace_linear_in_T_no_TxV(lib, name):
         assert sizes[-1] < 0.5 * 2 * w.T * w.V, (which, sizes)
     # the gradient-of-logits buffer stays within chunk x V bf16 (+ tile padding)
     bwd = kdkl.kd_kl_workspace_size(w.T, w.d, w.V, w.K, 1.0, w.chunk, 1)
-    per_token = 2 * 4 * w.K + 4 * w.d  # sorted teacher (id, p) + fp32 dH accumulator
+    # sorted teacher (id, p), the fp32 dH accumulator, and the compaction of
+    # the counted tokens (row maps and H's counted rows in bf16)
+    per_token = 2 * 4 * w.K + 4 * w.d + 2 * 4 + 2 * w.d
     g_budget = 2 * w.chunk * w.V * 1.07 + 2 * 256 * w.T + 2 * 128 * w.V
     assert bwd <= w.T * per_token + g_budget + (1 << 20)
 

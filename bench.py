@@ -34,8 +34,10 @@ METRIC = "fused chunked KL fwd+bwd tokens/s, % of BF16 tensor peak, peak HBM GiB
 WORKLOAD = "gptoss20b_32k"
 SPEC_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_KERNELS = ("fwd_lse_gemm", "bwd_grad_gemm", "dH_gemm", "dW_gemm", "fwd_lse_mix_gemm",
-                "bwd_grad_mix_gemm")
+# GEMM kernels and the GEMM-equivalents (2 N V d flops each) one step runs in
+# each: the backward's dW and dH share one launch per block
+GEMM_KERNELS = {"fwd_lse_gemm": 1, "bwd_grad_gemm": 1, "dH_gemm": 1, "dW_gemm": 1,
+                "dW_dH_gemm": 2, "fwd_lse_mix_gemm": 1, "bwd_grad_mix_gemm": 1}
 MIX_ALPHA, MIX_TAU_SQ = 0.5, True  # --path mix: alpha * tau^2 * KL + (1 - alpha) * CE
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -472,7 +474,8 @@ def run_kdkl(args):
         run_name = wname  # traffic is recorded for the plain workloads only
         dom_launches, dom_ms = rows[dom]
         if dom in GEMM_KERNELS:
-            per_launch_flops = 2.0 * n_counted * V * d * args.steps / dom_launches
+            per_launch_flops = (GEMM_KERNELS[dom] * 2.0 * n_counted * V * d * args.steps
+                                / dom_launches)
             achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
             peak = pk["bf16_tflops_sustained"]
             roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),

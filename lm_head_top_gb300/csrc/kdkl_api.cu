@@ -230,7 +230,6 @@ constexpr int kHeaderCounter0 = 16;
 constexpr int kHeaderCounters = 48;
 
 struct BwdPlan {
-  bool vocab_slabs;  // true: blocks are all tokens x a vocabulary slab
   int64_t Tb, Vb;    // block extent (tokens, vocabulary)
   int64_t Tb_pad, Vb_pad;
   int64_t n_tblocks, n_vblocks;
@@ -277,14 +276,22 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, 
   return f;
 }
 
-// own_teacher: the backward prepares the sorted teacher cache itself (sidx,
-// sp in its workspace); otherwise it reads the forward's.
-BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
-  BwdPlan b{};
-  const int64_t T = std::max<int64_t>(p.T, 1);
-  const double budget = (double)p.chunk * (double)p.V;  // gradient-of-logits elements
+// Block plans of the backward over the tokens x vocabulary plane, each block
+// within the chunk x V budget of the bf16 gradient-of-logits buffer.
+//   slabs:  all tokens x a vocabulary slab (T <= V), or chunk tokens x all
+//           vocabulary (T > V);
+//   2D:     about sqrt(budget) tokens x the vocabulary that fits.
+// Every block adds its partial dH into the fp32 dH accumulator (one
+// read-modify-write of T x d per vocabulary block after the first) and its
+// partial dW into dW (one of V x d per token block after the first); the plan
+// with the fewer such bytes is taken, 2D only when it saves a quarter.
+struct BlockPlan {
+  int64_t Tb, Vb, n_tblocks, n_vblocks;
+};
+
+BlockPlan slab_plan(const kd_kl_problem& p, int64_t T, double budget) {
+  BlockPlan b{};
   if (T <= p.V) {
-    b.vocab_slabs = true;
     b.Tb = T;
     int64_t vb_max = (int64_t)std::min<double>((double)p.V, std::floor(budget / (double)T));
     vb_max = std::max<int64_t>(vb_max, 256);
@@ -293,12 +300,49 @@ BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
     b.n_vblocks = ceil_div(p.V, b.Vb);
     b.n_tblocks = 1;
   } else {
-    b.vocab_slabs = false;
     b.Vb = p.V;
     b.Tb = std::min<int64_t>(round_up(std::min<int64_t>(p.chunk, T), BM), T);
     b.n_tblocks = ceil_div(T, b.Tb);
     b.n_vblocks = 1;
   }
+  return b;
+}
+
+BlockPlan square_plan(const kd_kl_problem& p, int64_t T, double budget) {
+  BlockPlan b{};
+  const int64_t tb = std::min<int64_t>(T, round_up((int64_t)std::sqrt(budget), 256));
+  b.n_tblocks = ceil_div(T, tb);
+  b.Tb = std::min<int64_t>(round_up(ceil_div(T, b.n_tblocks), 256), T);
+  b.n_tblocks = ceil_div(T, b.Tb);
+  int64_t vb_max = (int64_t)std::min<double>((double)p.V, std::floor(budget / (double)b.Tb));
+  vb_max = std::max<int64_t>(vb_max, 256);
+  b.n_vblocks = ceil_div(p.V, vb_max);
+  b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), 64), p.V);
+  b.n_vblocks = ceil_div(p.V, b.Vb);
+  return b;
+}
+
+double rmw_bytes(const BlockPlan& b, int64_t T, const kd_kl_problem& p) {
+  return 8.0 * (double)p.d *
+         ((double)(b.n_vblocks - 1) * (double)T + (double)(b.n_tblocks - 1) * (double)p.V);
+}
+
+// own_teacher: the backward prepares the sorted teacher cache itself (sidx,
+// sp in its workspace); otherwise it reads the forward's.
+BwdPlan plan_backward(const kd_kl_problem& p, bool own_teacher = true) {
+  BwdPlan b{};
+  const int64_t T = std::max<int64_t>(p.T, 1);
+  const double budget = (double)p.chunk * (double)p.V;  // gradient-of-logits elements
+  const BlockPlan slab = slab_plan(p, T, budget);
+  const BlockPlan sq = square_plan(p, T, budget);
+  const char* e2d = getenv("KDKL_BWD_2D");  // tuning: 1 / 0 forces the 2D / slab plan
+  const bool two_d = e2d ? (e2d[0] == '1')
+                         : (rmw_bytes(sq, T, p) <= 0.75 * rmw_bytes(slab, T, p));
+  const BlockPlan& bp = two_d ? sq : slab;
+  b.Tb = bp.Tb;
+  b.Vb = bp.Vb;
+  b.n_tblocks = bp.n_tblocks;
+  b.n_vblocks = bp.n_vblocks;
   b.Tb_pad = round_up(b.Tb, BM);
   b.Vb_pad = round_up(b.Vb, LOGIT_BN);
   size_t o = kHeaderBytes;
@@ -838,65 +882,92 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         KD_CUDA(launch_gemm(mix ? GEMM_BWD_GRAD_MIX : GEMM_BWD_GRAD, LOGIT_BN, pair, tmH_K, tmW_K,
                             sh, ep, status, grid, stream));
       }
-      // 2) dH[rows] (+)= G . W[cols]
-      {
-        CUtensorMap tmG_K;
-        if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM)) return KD_ERR_CUDA;
-        GemmShape sh{};
-        sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(rows, tile_m);
-        sh.n_tiles = dn_tiles;
-        sh.nsplit = dn_tiles;
-        sh.group_m = 1;  // m-major: an m-tile's output tiles run side by side
-        sh.units = sh.m_tiles * sh.nsplit;
-        sh.k_blocks = (int)ceil_div(cols, BK);
-        sh.b_k0 = col0;
-        sh.counter = next_counter();
-        if (compact) {
-          sh.dyn_rows = n_count;
-          sh.dyn_base = row0;
-          sh.dyn_cap = rows;
-          sh.dyn_dim = 0;  // M: the block's counted tokens
-        }
-        EpiParams ep{};
-        ep.out = dH_acc + (int64_t)row0 * d;
-        ep.ldo = d;
-        ep.out_rows = rows;
-        ep.out_cols = d;
-        ep.accumulate = vb > 0 ? 1 : 0;
-        const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
-        if (log_plan() && vb == 0 && tb == 0) print_plan("dH", pair, procs, sh, grid);
-        KD_CUDA(launch_gemm(GEMM_DH, out_bn, pair, tmG_K, tmW_MN, sh, ep, status, grid, stream));
+      // 2) dH[rows] (+)= G . W[cols] and 3) dW[cols] (+)= G^T . H[rows]: one
+      // launch whose units run dW's (long: K = the block's tokens) first, then
+      // dH's (short: K = the slab's columns), so the short units fill the
+      // tail of the long ones. Each output element still gets one store or
+      // one add per launch, in stream order: deterministic.
+      CUtensorMap tmG_K, tmG_MN;
+      if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM) ||
+          !encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK))
+        return KD_ERR_CUDA;
+      GemmShape sh_dh{};
+      sh_dh.inject_stall = stall;
+      sh_dh.m_tiles = (int)ceil_div(rows, tile_m);
+      sh_dh.n_tiles = dn_tiles;
+      sh_dh.nsplit = dn_tiles;
+      sh_dh.group_m = 1;  // m-major: an m-tile's output tiles run side by side
+      sh_dh.units = sh_dh.m_tiles * sh_dh.nsplit;
+      sh_dh.k_blocks = (int)ceil_div(cols, BK);
+      sh_dh.b_k0 = col0;
+      if (compact) {
+        sh_dh.dyn_rows = n_count;
+        sh_dh.dyn_base = row0;
+        sh_dh.dyn_cap = rows;
+        sh_dh.dyn_dim = 0;  // M: the block's counted tokens
       }
-      // 3) dW[cols] (+)= G^T . H[rows]
-      {
-        CUtensorMap tmG_MN;
-        if (!encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK)) return KD_ERR_CUDA;
-        GemmShape sh{};
-        sh.inject_stall = stall;
-        sh.m_tiles = (int)ceil_div(cols, tile_m);
-        sh.n_tiles = dn_tiles;
-        sh.nsplit = dn_tiles;
-        sh.group_m = 1;
-        sh.units = sh.m_tiles * sh.nsplit;
-        sh.k_blocks = (int)ceil_div(rows, BK);
-        sh.b_k0 = row0;
-        sh.counter = next_counter();
-        if (compact) {
-          sh.dyn_rows = n_count;
-          sh.dyn_base = row0;
-          sh.dyn_cap = rows;
-          sh.dyn_dim = 1;  // K: the block's counted tokens
+      EpiParams ep_dh{};
+      ep_dh.out = dH_acc + (int64_t)row0 * d;
+      ep_dh.ldo = d;
+      ep_dh.out_rows = rows;
+      ep_dh.out_cols = d;
+      ep_dh.accumulate = vb > 0 ? 1 : 0;
+      GemmShape sh_dw{};
+      sh_dw.inject_stall = stall;
+      sh_dw.m_tiles = (int)ceil_div(cols, tile_m);
+      sh_dw.n_tiles = dn_tiles;
+      sh_dw.nsplit = dn_tiles;
+      sh_dw.group_m = 1;
+      sh_dw.units = sh_dw.m_tiles * sh_dw.nsplit;
+      sh_dw.k_blocks = (int)ceil_div(rows, BK);
+      sh_dw.b_k0 = row0;
+      if (compact) {
+        sh_dw.dyn_rows = n_count;
+        sh_dw.dyn_base = row0;
+        sh_dw.dyn_cap = rows;
+        sh_dw.dyn_dim = 1;  // K: the block's counted tokens
+      }
+      EpiParams ep_dw{};
+      ep_dw.out = dW + (int64_t)col0 * d;
+      ep_dw.ldo = d;
+      ep_dw.out_rows = cols;
+      ep_dw.out_cols = d;
+      ep_dw.accumulate = (accumulate_dW || tb > 0) ? 1 : 0;
+      // One launch pays when a separate one would leave much of its last wave
+      // idle (wave efficiency < 0.9: e.g. dW of narrow vocabulary slabs); the
+      // job with the longer units goes first. Otherwise two launches, which
+      // measured faster (their units start together and share operand tiles
+      // in L2; 45.7 vs 47.4 ms per step at 16K tokens of the GPT-OSS-like head).
+      auto wave_eff = [&](int units) {
+        const double w = (double)units / procs;
+        return w / std::ceil(w);
+      };
+      const char* dual_env = getenv("KDKL_DUAL_DHDW");  // 1: always one launch, 0: never
+      const bool dual = dual_env ? dual_env[0] == '1'
+                                 : (std::min(wave_eff(sh_dw.units), wave_eff(sh_dh.units)) < 0.9);
+      if (!dual) {
+        sh_dh.counter = next_counter();
+        int grid = cta_per_proc * (int)std::min<int64_t>(sh_dh.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) print_plan("dH", pair, procs, sh_dh, grid);
+        KD_CUDA(launch_gemm(GEMM_DH, out_bn, pair, tmG_K, tmW_MN, sh_dh, ep_dh, status, grid,
+                            stream));
+        sh_dw.counter = next_counter();
+        grid = cta_per_proc * (int)std::min<int64_t>(sh_dw.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) print_plan("dW", pair, procs, sh_dw, grid);
+        KD_CUDA(launch_gemm(GEMM_DW, out_bn, pair, tmG_MN, tmH_MN, sh_dw, ep_dw, status, grid,
+                            stream));
+      } else {
+        // the launch's one counter, read from job 0's shape
+        sh_dw.counter = sh_dh.counter = next_counter();
+        const int grid =
+            cta_per_proc * (int)std::min<int64_t>((int64_t)sh_dw.units + sh_dh.units, procs);
+        if (log_plan() && vb == 0 && tb == 0) {
+          print_plan("dW (job 0)", pair, procs, sh_dw, grid);
+          print_plan("dH (job 1)", pair, procs, sh_dh, grid);
         }
-        EpiParams ep{};
-        ep.out = dW + (int64_t)col0 * d;
-        ep.ldo = d;
-        ep.out_rows = cols;
-        ep.out_cols = d;
-        ep.accumulate = (accumulate_dW || tb > 0) ? 1 : 0;
-        const int grid = cta_per_proc * (int)std::min<int64_t>(sh.units, procs);
-        if (log_plan() && vb == 0 && tb == 0) print_plan("dW", pair, procs, sh, grid);
-        KD_CUDA(launch_gemm(GEMM_DW, out_bn, pair, tmG_MN, tmH_MN, sh, ep, status, grid, stream));
+        const bool dh_first = sh_dh.k_blocks > sh_dw.k_blocks;  // longer units first
+        KD_CUDA(launch_gemm_dw_dh(pair, dh_first, tmG_MN, tmH_MN, sh_dw, ep_dw, tmG_K, tmW_MN,
+                                  sh_dh, ep_dh, status, grid, stream));
       }
     }
   }

@@ -136,4 +136,13 @@ cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA
                         const GemmShape& sh, const EpiParams& ep, int* status, int grid,
                         cudaStream_t stream);
 
+// dW (A = G^T, B = H, both MN-major) and dH (A = G K-major, B = W MN-major)
+// of one backward block in one persistent launch, their units in one
+// sequence: dW's first, or dH's first when dh_first. 256-wide N tiles.
+cudaError_t launch_gemm_dw_dh(bool pair, bool dh_first, const CUtensorMap& tmG_MN,
+                              const CUtensorMap& tmH_MN, const GemmShape& sh_dw,
+                              const EpiParams& ep_dw, const CUtensorMap& tmG_K,
+                              const CUtensorMap& tmW_MN, const GemmShape& sh_dh,
+                              const EpiParams& ep_dh, int* status, int grid, cudaStream_t stream);
+
 }  // namespace kdkl

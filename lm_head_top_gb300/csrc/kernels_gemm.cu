@@ -12,11 +12,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR>
+template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR, bool DUAL>
 cudaError_t launch_one(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                       const GemmShape& sh, const EpiParams& ep, int* status, int grid,
-                       cudaStream_t stream) {
-  auto kern = tc_gemm_kernel<EPI, A_MN, B_MN, BN, PAIR>;
+                       const CUtensorMap& tmA1, const CUtensorMap& tmB1, const GemmShape& sh,
+                       const GemmShape& sh1, const EpiParams& ep, const EpiParams& ep1,
+                       int* status, int grid, cudaStream_t stream) {
+  auto kern = tc_gemm_kernel<EPI, A_MN, B_MN, BN, PAIR, DUAL>;
   constexpr int smem = TileCfg<BN, PAIR>::SMEM_BYTES;
   // Per device and instantiation; concurrent first calls may both set the
   // attribute, which is harmless (same value).
@@ -32,18 +33,22 @@ cudaError_t launch_one(const char* name, const CUtensorMap& tmA, const CUtensorM
   }
   if (PAIR)
     return launch_kernel_cluster(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)smem, stream,
-                                 2u, tmA, tmB, sh, ep, status);
+                                 2u, tmA, tmB, tmA1, tmB1, sh, sh1, ep, ep1, status);
   return launch_kernel(name, kern, dim3(grid), dim3(GEMM_THREADS), (size_t)smem, stream, tmA,
-                       tmB, sh, ep, status);
+                       tmB, tmA1, tmB1, sh, sh1, ep, ep1, status);
 }
 
+// One job per launch: the second job's parameters repeat the first's and are
+// not read.
 template <int EPI, bool A_MN, bool B_MN, int BN>
 cudaError_t launch_pick(bool pair, const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const GemmShape& sh, const EpiParams& ep, int* status, int grid,
                         cudaStream_t stream) {
   if (pair)
-    return launch_one<EPI, A_MN, B_MN, BN, true>(name, tmA, tmB, sh, ep, status, grid, stream);
-  return launch_one<EPI, A_MN, B_MN, BN, false>(name, tmA, tmB, sh, ep, status, grid, stream);
+    return launch_one<EPI, A_MN, B_MN, BN, true, false>(name, tmA, tmB, tmA, tmB, sh, sh, ep, ep,
+                                                        status, grid, stream);
+  return launch_one<EPI, A_MN, B_MN, BN, false, false>(name, tmA, tmB, tmA, tmB, sh, sh, ep, ep,
+                                                       status, grid, stream);
 }
 
 }  // namespace
@@ -56,7 +61,7 @@ int pair_max_active_clusters() {
   if (known > 0) return known;
   // Every pair instantiation has the same block size and shared memory, so one
   // of them stands for all.
-  auto kern = tc_gemm_kernel<EPI_LSE, false, false, LOGIT_BN, true>;
+  auto kern = tc_gemm_kernel<EPI_LSE, false, false, LOGIT_BN, true, false>;
   constexpr int smem = TileCfg<LOGIT_BN, true>::SMEM_BYTES;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
@@ -113,6 +118,30 @@ cudaError_t launch_gemm(GemmKind kind, int bn, bool pair, const CUtensorMap& tmA
                                                      grid, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_dw_dh(bool pair, bool dh_first, const CUtensorMap& tmG_MN,
+                              const CUtensorMap& tmH_MN, const GemmShape& sh_dw,
+                              const EpiParams& ep_dw, const CUtensorMap& tmG_K,
+                              const CUtensorMap& tmW_MN, const GemmShape& sh_dh,
+                              const EpiParams& ep_dh, int* status, int grid, cudaStream_t stream) {
+  if (pair && (grid % 2) != 0) return cudaErrorInvalidValue;
+  if (dh_first) {  // job 0 = dH (A K-major), job 1 = dW
+    if (pair)
+      return launch_one<EPI_STORE, false, true, 256, true, true>(
+          "dW_dH_gemm", tmG_K, tmW_MN, tmG_MN, tmH_MN, sh_dh, sh_dw, ep_dh, ep_dw, status, grid,
+          stream);
+    return launch_one<EPI_STORE, false, true, 256, false, true>(
+        "dW_dH_gemm", tmG_K, tmW_MN, tmG_MN, tmH_MN, sh_dh, sh_dw, ep_dh, ep_dw, status, grid,
+        stream);
+  }
+  if (pair)  // job 0 = dW (A MN-major), job 1 = dH
+    return launch_one<EPI_STORE, true, true, 256, true, true>(
+        "dW_dH_gemm", tmG_MN, tmH_MN, tmG_K, tmW_MN, sh_dw, sh_dh, ep_dw, ep_dh, status, grid,
+        stream);
+  return launch_one<EPI_STORE, true, true, 256, false, true>(
+      "dW_dH_gemm", tmG_MN, tmH_MN, tmG_K, tmW_MN, sh_dw, sh_dh, ep_dw, ep_dh, status, grid,
+      stream);
 }
 
 }  // namespace kdkl

@@ -310,10 +310,33 @@ __device__ __forceinline__ int lower_bound_row(const int32_t* row, int K, int v)
   return lo;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR>
+// Shrinks a shape to the rows counted on the device (see GemmShape::dyn_rows);
+// returns the live extent along M (or -1 when M is not shrunk).
+template <int TILE_M>
+__device__ __forceinline__ int shrink_shape(GemmShape& sh) {
+  if (!sh.dyn_rows) return -1;
+  const int a = max(0, min(*sh.dyn_rows - sh.dyn_base, sh.dyn_cap));
+  if (sh.dyn_dim == 0) {
+    sh.m_tiles = min(sh.m_tiles, (a + TILE_M - 1) / TILE_M);
+    sh.units = sh.m_tiles * sh.nsplit;
+    return a;
+  }
+  sh.k_blocks = min(sh.k_blocks, (a + BK - 1) / BK);
+  return -1;
+}
+
+// DUAL: two store GEMMs in one persistent launch, their units in one
+// sequence: job 0 (maps tmA/tmB, shape sh, output ep; A as A_MN) and then job
+// 1 (tmA1/tmB1, sh1, ep1; A the other way round, B as B_MN). The backward runs
+// dW and dH of a block this way (the tail of the first job's units is filled
+// by the second job's).
+template <int EPI, bool A_MN, bool B_MN, int BN, bool PAIR, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmShape sh_in, const EpiParams ep, int* status) {
+                   const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB1, const GemmShape sh_in,
+                   const GemmShape sh1_in, const EpiParams ep, const EpiParams ep1, int* status) {
+  static_assert(!DUAL || EPI == EPI_STORE, "two jobs per launch only for store epilogues");
   using Cfg = TileCfg<BN, PAIR>;
   constexpr bool IS_LSE = EPI == EPI_LSE || EPI == EPI_LSE_MIX;
   constexpr bool IS_GRAD = EPI == EPI_GRAD || EPI == EPI_GRAD_MIX;
@@ -346,23 +369,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   auto ufull_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + i); };
   auto uempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + NSLOT + i); };
 
-  // Every role shrinks the shape to the live rows the same way, so they all
+  // Every role shrinks the shapes to the live rows the same way, so they all
   // see the same units and K steps.
   GemmShape sh = sh_in;
+  GemmShape sh1 = sh1_in;
   int live_rows = IS_LSE || IS_GRAD ? ep.rows : 0;  // rows whose token counts
-  if (sh.dyn_rows) {
-    const int a = max(0, min(*sh.dyn_rows - sh.dyn_base, sh.dyn_cap));
-    if (sh.dyn_dim == 0) {
-      sh.m_tiles = min(sh.m_tiles, (a + TILE_M - 1) / TILE_M);
-      sh.units = sh.m_tiles * sh.nsplit;
-      live_rows = min(live_rows, a);
-    } else {
-      sh.k_blocks = min(sh.k_blocks, (a + BK - 1) / BK);
-    }
+  {
+    const int a = shrink_shape<TILE_M>(sh);
+    if (a >= 0) live_rows = min(live_rows, a);
+    if (DUAL) shrink_shape<TILE_M>(sh1);
   }
-  // No K steps (no live token in a dW launch): no copies and no MMAs; the
-  // epilogue writes zeros (or adds nothing) without touching TMEM.
-  const bool no_k = sh.k_blocks == 0;
+  const int units0 = sh.units;
+  const int units_all = units0 + (DUAL ? sh1.units : 0);
+  // Per unit: its job's shape, the unit within that job, and A's layout.
+  auto job_of = [&](int u, const GemmShape*& js, int& uu, bool& a_mn) {
+    const bool j1 = DUAL && u >= units0;
+    js = j1 ? &sh1 : &sh;
+    uu = j1 ? u - units0 : u;
+    a_mn = j1 ? !A_MN : A_MN;
+    return j1;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -394,6 +420,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (DUAL) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
   }
   if (warp == 1) {
     __syncwarp();
@@ -463,7 +493,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          u = next < sh.units ? next : -1;
+          u = next < units_all ? next : -1;
           if (u >= 0) next = dyn ? atomicAdd(sh.counter, 1) : next + groups;
           unit_slot[slot] = u;
           if (PAIR) {
@@ -479,12 +509,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           release_unit(uq);
         }
         if (u < 0) break;
+        const GemmShape* js;
+        int uu;
+        bool a_mn;
+        const bool j1 = job_of(u, js, uu, a_mn);
+        const CUtensorMap* ta = j1 ? &tmA1 : &tmA;
+        const CUtensorMap* tb = j1 ? &tmB1 : &tmB;
         int m, s, nb, ne;
-        unit_coords(sh, u, m, s, nb, ne);
-        const int a_row = sh.a_m0 + m * TILE_M + (int)rank * BM;
+        unit_coords(*js, uu, m, s, nb, ne);
+        const int a_row = js->a_m0 + m * TILE_M + (int)rank * BM;
         for (int n = nb; ok && n < ne; ++n) {
-          const int b_row = sh.b_n0 + n * BN + (int)rank * B_ROWS;
-          for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          const int b_row = js->b_n0 + n * BN + (int)rank * B_ROWS;
+          for (int kb = 0; kb < js->k_blocks; ++kb) {
             if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status, limit)) {
               ok = false;
               break;
@@ -500,19 +536,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               else
                 tma_load_2d(dst, tm, fb, x, y);
             };
-            if (!A_MN) {
-              load(a_dst, &tmA, sh.a_k0 + kc, a_row);
+            if (!a_mn) {
+              load(a_dst, ta, js->a_k0 + kc, a_row);
             } else {
 #pragma unroll
               for (int a = 0; a < BM / 64; ++a)
-                load(a_dst + a * MN_ATOM_BYTES, &tmA, a_row + 64 * a, sh.a_k0 + kc);
+                load(a_dst + a * MN_ATOM_BYTES, ta, a_row + 64 * a, js->a_k0 + kc);
             }
             if (!B_MN) {
-              load(b_dst, &tmB, sh.b_k0 + kc, b_row);
+              load(b_dst, tb, js->b_k0 + kc, b_row);
             } else {
 #pragma unroll
               for (int a = 0; a < B_ROWS / 64; ++a)
-                load(b_dst + a * MN_ATOM_BYTES, &tmB, b_row + 64 * a, sh.b_k0 + kc);
+                load(b_dst + a * MN_ATOM_BYTES, tb, b_row + 64 * a, js->b_k0 + kc);
             }
             ++fills;
             if (++stage == STAGES) {
@@ -534,7 +570,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
+      constexpr uint32_t idesc0 = idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
+      constexpr uint32_t idesc1 = idesc_bf16_f32(TILE_M, BN, !A_MN, B_MN);  // DUAL job 1
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -545,9 +582,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (!take_unit(uq, u)) break;
         release_unit(uq);
         if (u < 0) break;
-        if (no_k) continue;  // nothing to multiply: the epilogue writes zeros
+        const GemmShape* js;
+        int uu;
+        bool a_mn;
+        const bool j1 = job_of(u, js, uu, a_mn);
+        // No K steps (no counted token in a dW launch): nothing to multiply;
+        // the epilogue writes zeros without touching TMEM.
+        if (js->k_blocks == 0) continue;
+        const uint32_t idesc = j1 ? idesc1 : idesc0;
         int m, s, nb, ne;
-        unit_coords(sh, u, m, s, nb, ne);
+        unit_coords(*js, uu, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
           const bool freed = PAIR ? mbar_wait_cluster_bounded(tempty_bar(acc), acc_phase ^ 1u,
                                                               abort_flag, status, limit)
@@ -559,7 +603,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-          for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          for (int kb = 0; kb < js->k_blocks; ++kb) {
             if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status, limit)) {
               ok = false;
               break;
@@ -569,7 +613,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t b_base = smem_u32(sB + stage * B_STAGE_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t ad = A_MN ? sdesc_sw128(a_base + k * 2048, MN_ATOM_BYTES, 1024)
+              const uint64_t ad = a_mn ? sdesc_sw128(a_base + k * 2048, MN_ATOM_BYTES, 1024)
                                        : sdesc_sw128(a_base + k * 32, 16, 1024);
               const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                        : sdesc_sw128(b_base + k * 32, 16, 1024);
@@ -663,8 +707,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       __syncwarp();  // every lane has read the slot before it is released
       if (lane == 0) release_unit(uq);
       if (u < 0) break;
+      const GemmShape* js;
+      int uu;
+      bool a_mn_unused;
+      const bool j1 = job_of(u, js, uu, a_mn_unused);
+      const EpiParams& eo = j1 ? ep1 : ep;  // the unit's output (store epilogues)
+      const bool no_k = js->k_blocks == 0;  // zeros, no TMEM (see the MMA role)
       int m, s, nb, ne;
-      unit_coords(sh, u, m, s, nb, ne);
+      unit_coords(*js, uu, m, s, nb, ne);
       const int r = m * TILE_M + (int)rank * BM + r_in_tile;  // row within this launch
       // per-unit row state
       float run_max = -INFINITY, run_sum = 0.f, dot = 0.f;
@@ -759,7 +809,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (IS_LSE || IS_GRAD || EPI == EPI_TOPK) {
             if (cl >= ep.cols) break;  // warp-uniform
           } else {
-            if (cl >= ep.out_cols) break;
+            if (cl >= eo.out_cols) break;
           }
           if (EPI == EPI_TOPK) {
             // room for this piece's 32 possible appends in every row of the warp
@@ -882,9 +932,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
             }
           } else {  // EPI_STORE
-            if (r < ep.out_rows) {
-              float* dst = ep.out + (long long)r * ep.ldo + cl;
-              const int nvalid = min(32, ep.out_cols - cl);  // multiple of 4
+            if (r < eo.out_rows) {
+              float* dst = eo.out + (long long)r * eo.ldo + cl;
+              const int nvalid = min(32, eo.out_cols - cl);  // multiple of 4
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 if (4 * j < nvalid) {
@@ -892,7 +942,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   // Accumulate with a vector reduction: every element gets
                   // exactly one add per launch and launches are stream-ordered,
                   // so the sum order is fixed (deterministic).
-                  if (ep.accumulate)
+                  if (eo.accumulate)
                     red_add_f32x4(dst + 4 * j, o);
                   else
                     *reinterpret_cast<float4*>(dst + 4 * j) = o;

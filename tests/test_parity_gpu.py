@@ -158,7 +158,7 @@ def test_timing_and_launch_count(kdkl):
     rows = kdkl.kd_timing_end()
     names = {r[0] for r in rows}
     assert {"teacher_prep", "fwd_lse_gemm", "lse_combine", "loss_finalize", "bwd_grad_gemm",
-            "dH_gemm", "dW_gemm", "f32_to_bf16"} <= names
+            "dW_dH_gemm", "f32_to_bf16", "mask_scan", "gather_rows"} <= names
     assert kdkl.kd_launch_count() - before == sum(r[1] for r in rows)
     assert all(r[2] > 0 for r in rows)
 

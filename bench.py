@@ -307,6 +307,8 @@ def apply_overrides(w, args):
     kw = {}
     if args.tokens:
         kw["T"] = args.tokens
+    if args.vocab:
+        kw["V"] = args.vocab
     if args.K:
         kw["K"] = args.K
     if args.tau:
@@ -316,7 +318,7 @@ def apply_overrides(w, args):
     if not kw:
         return w, w.name
     w2 = w.with_(**kw)
-    return w2, "%s_T%d_K%d_tau%g_chunk%d" % (w.name, w2.T, w2.K, w2.tau, w2.chunk)
+    return w2, "%s_T%d_V%d_K%d_tau%g_chunk%d" % (w.name, w2.T, w2.V, w2.K, w2.tau, w2.chunk)
 
 
 def run_kdkl(args):
@@ -839,6 +841,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0,
                     help="input seed (rank r of a multi-GPU run uses seed + r)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="override V (profiling cases: a smaller vocabulary with a larger chunk "
+                         "keeps the backward's per-launch shapes)")
     ap.add_argument("--K", type=int, default=0, help="override K (config sweeps)")
     ap.add_argument("--tau", type=float, default=0.0, help="override the temperature")
     ap.add_argument("--chunk", type=int, default=0, help="override chunk")

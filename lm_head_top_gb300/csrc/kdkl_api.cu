@@ -820,6 +820,12 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
   // (more operand bytes per MAC), so 256 is used throughout.
   const int out_bn = 256;
   const int dn_tiles = (int)ceil_div(d, out_bn);
+  // When the last column tile of d holds at most half a tile (d = 2880:
+  // 11 x 256 + 64), it runs as a 128-wide tile (KDKL_NARROW_LAST=0 keeps the
+  // full width, to compare).
+  const char* nl_env = getenv("KDKL_NARROW_LAST");
+  const int narrow_last =
+      (d % out_bn != 0 && d % out_bn <= out_bn / 2 && !(nl_env && nl_env[0] == '0')) ? 1 : 0;
   const int stall = inject_stall_from_env();
   for (int64_t tb = 0; tb < b.n_tblocks; ++tb) {
     const int row0 = (int)(tb * b.Tb);
@@ -900,6 +906,7 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
       sh_dh.units = sh_dh.m_tiles * sh_dh.nsplit;
       sh_dh.k_blocks = (int)ceil_div(cols, BK);
       sh_dh.b_k0 = col0;
+      sh_dh.narrow_last = narrow_last;
       if (compact) {
         sh_dh.dyn_rows = n_count;
         sh_dh.dyn_base = row0;
@@ -921,6 +928,7 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
       sh_dw.units = sh_dw.m_tiles * sh_dw.nsplit;
       sh_dw.k_blocks = (int)ceil_div(rows, BK);
       sh_dw.b_k0 = row0;
+      sh_dw.narrow_last = narrow_last;
       if (compact) {
         sh_dw.dyn_rows = n_count;
         sh_dw.dyn_base = row0;

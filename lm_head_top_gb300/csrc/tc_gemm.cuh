@@ -100,6 +100,10 @@ struct GemmShape {
   // m_tiles / units or k_blocks shrink to it before any role starts.
   const int* dyn_rows;
   int dyn_base, dyn_cap, dyn_dim;
+  // Nonzero (B MN-major only): the last n-tile holds at most BN/2 columns of
+  // B (d = 2880 is 11 tiles of 256 and 64 columns), so its MMAs run N = BN/2
+  // and each CTA copies half of its B rows: half the padded work and B bytes.
+  int narrow_last;
 };
 
 // n-tile range [nb, ne) of split s.
@@ -519,14 +523,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         unit_coords(*js, uu, m, s, nb, ne);
         const int a_row = js->a_m0 + m * TILE_M + (int)rank * BM;
         for (int n = nb; ok && n < ne; ++n) {
-          const int b_row = js->b_n0 + n * BN + (int)rank * B_ROWS;
+          const bool narrow = B_MN && js->narrow_last && n == js->n_tiles - 1;
+          const int b_rows = narrow ? B_ROWS / 2 : B_ROWS;  // B rows this CTA copies
+          const int b_row = js->b_n0 + n * BN + (int)rank * b_rows;
+          const uint32_t stage_bytes = (uint32_t)(A_STAGE_BYTES + b_rows * BK * 2);
           for (int kb = 0; kb < js->k_blocks; ++kb) {
             if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status, limit)) {
               ok = false;
               break;
             }
             const uint32_t fb = full_leader0 + 8u * stage;
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), (PAIR ? 2u : 1u) * stage_bytes);
             const uint32_t a_dst = smem_u32(sA + stage * A_STAGE_BYTES);
             const uint32_t b_dst = smem_u32(sB + stage * B_STAGE_BYTES);
             const int kc = kb * BK;
@@ -546,8 +553,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (!B_MN) {
               load(b_dst, tb, js->b_k0 + kc, b_row);
             } else {
-#pragma unroll
-              for (int a = 0; a < B_ROWS / 64; ++a)
+              for (int a = 0; a < b_rows / 64; ++a)
                 load(b_dst + a * MN_ATOM_BYTES, tb, b_row + 64 * a, js->b_k0 + kc);
             }
             ++fills;
@@ -593,6 +599,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int m, s, nb, ne;
         unit_coords(*js, uu, m, s, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
+          // the narrow last tile (see GemmShape::narrow_last) multiplies N = BN/2
+          const bool narrow = B_MN && js->narrow_last && n == js->n_tiles - 1;
+          const uint32_t idesc_n =
+              narrow ? idesc_bf16_f32(TILE_M, BN / 2, a_mn, B_MN) : idesc;
           const bool freed = PAIR ? mbar_wait_cluster_bounded(tempty_bar(acc), acc_phase ^ 1u,
                                                               abort_flag, status, limit)
                                   : mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u,
@@ -618,9 +628,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                        : sdesc_sw128(b_base + k * 32, 16, 1024);
               if (PAIR)
-                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc_n, (kb | k) != 0 ? 1u : 0u);
               else
-                tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                tc_mma_bf16(d_tmem, ad, bd, idesc_n, (kb | k) != 0 ? 1u : 0u);
             }
             if (PAIR)
               tc_commit_pair_multicast(empty_bar(stage), 0x3);

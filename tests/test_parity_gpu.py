@@ -65,9 +65,12 @@ def test_small_workload(kdkl):
     (64, 32, 48, 48, 16, 0.5),
     # K = 512 (largest), V just above
     (40, 48, 600, 512, 7, 1.0),
-    # hidden sizes that take 192-wide dH / dW tiles (multiple of 192, not of 256)
+    # hidden sizes whose last 256-wide dH / dW column tile is at most half
+    # full: that tile runs 128 wide
     (200, 576, 900, 10, 70, 1.0),
     (129, 384, 777, 3, 129, 1.5),
+    # last column tile more than half full: it stays 256 wide
+    (150, 448, 900, 10, 70, 1.0),
 ])
 def test_ragged_shapes(kdkl, shape):
     T, d, V, K, chunk, tau = shape
@@ -232,3 +235,27 @@ def test_mask_compaction_across_scan_tiles(kdkl):
     m[65530:65540] = 1                             # counted tokens around the second edge
     x["mask"] = torch.from_numpy(m)
     _compare(run_gpu(kdkl, x, w.tau, w.chunk), x, w.tau)
+
+
+@pytest.mark.parametrize("shape", [
+    # T, d, V, K, chunk : d = 2880 is 11 column tiles of 256 and one of 64
+    (512, 2880, 5000, 32, 2048),
+    (300, 320, 5000, 8, 1000),
+    (64, 72, 900, 4, 300),
+])
+def test_narrow_last_column_tile(kdkl, shape, monkeypatch):
+    """The last dH / dW column tile, when at most half full, multiplies
+    N = 128 instead of 256 and copies half the B rows. Each output element
+    still sums the same products in the same k order, so dH and dW equal
+    those of the full-width tile bit for bit, and both match the oracle."""
+    T, d, V, K, chunk = shape
+    w = WORKLOADS["small"].with_(T=T, d=d, V=V, K=K, chunk=chunk, tau=1.0,
+                                 seq_len=max(T // 4, 1), pad_frac=0.1)
+    x = make_inputs(w, seed=31)
+    runs = {}
+    for narrow in ("0", "1"):
+        monkeypatch.setenv("KDKL_NARROW_LAST", narrow)
+        runs[narrow] = run_gpu(kdkl, x, w.tau, w.chunk, grad_loss=0.5)
+    for key in ("dH", "dW"):
+        assert np.array_equal(runs["0"][key], runs["1"][key]), key
+    _compare(runs["1"], x, w.tau, grad_loss=0.5)

@@ -10,6 +10,7 @@
 // enough to run at scale", section "Two system changes" (top-100 cache per
 // position; the sparse teacher of the forward-chunked and fused variants).
 #include <cuda_bf16.h>
+#include <float.h>
 #include <stdint.h>
 #include <stdlib.h>
 
@@ -25,11 +26,12 @@ namespace kdkl {
 // a warp, lane l holding elements l*E .. l*E+E-1 of the row padded to
 // N = L*E (a power of two >= K). The row is read from global memory once, into
 // registers; the teacher softmax, its entropy term and the validation run
-// there. The (id, p) pairs are then ordered by id with a bitonic network on
-// packed keys (id, original position): the first log2(E) levels of every
-// merge stay inside a lane, the rest exchange keys with __shfl_xor_sync, and
-// p follows through a per-row shared-memory slot indexed by the original
-// position. Packed keys are distinct, so the network needs no tie rule.
+// there. The (id, p) pairs are then ordered by id with a bitonic sorting
+// network on packed keys (id, original position): exchanges between
+// positions closer than E stay inside a lane, the rest exchange keys with
+// __shfl_xor_sync, and p follows through a per-row shared-memory slot
+// indexed by the original position. Packed keys are distinct, so the network
+// needs no tie rule.
 constexpr int PREP_THREADS = 256;
 
 template <int N>
@@ -59,6 +61,15 @@ __device__ __forceinline__ uint32_t shfl_key(uint32_t v, int o) {
 }
 __device__ __forceinline__ unsigned long long shfl_key(unsigned long long v, int o) {
   return __shfl_xor_sync(0xffffffffu, v, o);
+}
+
+__device__ __forceinline__ uint32_t kmin(uint32_t a, uint32_t b) { return min(a, b); }
+__device__ __forceinline__ uint32_t kmax(uint32_t a, uint32_t b) { return max(a, b); }
+__device__ __forceinline__ unsigned long long kmin(unsigned long long a, unsigned long long b) {
+  return min(a, b);
+}
+__device__ __forceinline__ unsigned long long kmax(unsigned long long a, unsigned long long b) {
+  return max(a, b);
 }
 
 // Sum / max over the L lanes of one row (xor offsets below L stay in the row).
@@ -129,14 +140,14 @@ __global__ void __launch_bounds__(PREP_THREADS)
     }
   }
 
-  // ---- validation, max of a = logit / tau
+  // ---- validation, max of a = logit / tau. Padding and the slots of a row
+  // past T hold (id 0, -inf), which pass both checks.
   bool bad_id = false, bad_logit = false;
   float amax = -INFINITY;
 #pragma unroll
   for (int j = 0; j < E; ++j) {
-    const bool in = live && l * E + j < K;
-    bad_id |= in && (id[j] < 0 || id[j] >= V);
-    bad_logit |= in && ((a[j] != a[j]) || (a[j] == INFINITY));
+    bad_id |= (uint32_t)id[j] >= (uint32_t)V;  // negative ids wrap above V
+    bad_logit |= !(a[j] < INFINITY);           // NaN or +inf
     amax = fmaxf(amax, a[j]);
   }
   amax = row_max<L>(amax);
@@ -150,27 +161,30 @@ __global__ void __launch_bounds__(PREP_THREADS)
   }
 
   // ---- teacher softmax over the K entries and sum p log p (0 log 0 = 0).
-  // __expf and a reciprocal (a few ulp; the loss tolerance is 1e-3 relative):
-  // the kernel is bound by instruction issue, and the accurate forms cost 15 %.
+  // With d = a - max and S = sum exp(d): p = exp(d) / S and
+  // sum p log p = sum exp(d) d / S - log S. An entry at -inf has exp(d) = 0
+  // and its d is clamped to -FLT_MAX, so it adds exactly 0. A row without a
+  // finite entry (an error, reported above) gets p = 0 and 0.
+  // __expf, __logf and a reciprocal (a few ulp; the loss tolerance is 1e-3
+  // relative): the kernel is bound by its integer pipe (the sort), and every
+  // instruction saved here counts.
+  const float amax_s = no_finite ? 0.f : amax;
   float e[E];
-  float sum = 0.f;
+  float sum = 0.f, ed = 0.f;
 #pragma unroll
   for (int j = 0; j < E; ++j) {
-    e[j] = no_finite ? 0.f : __expf(a[j] - amax);  // 0 for -inf and padding
+    const float dj = a[j] - amax_s;
+    e[j] = __expf(dj);  // 0 for -inf and padding
     sum += e[j];
+    ed = fmaf(e[j], fmaxf(dj, -FLT_MAX), ed);
   }
   sum = row_sum<L>(sum);
-  const float log_sum = logf(sum);
-  const float inv_sum = 1.0f / sum;
-  float h = 0.f;
+  ed = row_sum<L>(ed);
+  const float inv_sum = no_finite ? 0.f : 1.0f / sum;
+  const float h = no_finite ? 0.f : fmaf(ed, inv_sum, -__logf(sum));
   float* ps = p_slot + row * N;
 #pragma unroll
-  for (int j = 0; j < E; ++j) {
-    const float p = no_finite ? 0.f : e[j] * inv_sum;
-    if (p > 0.f) h += p * ((a[j] - amax) - log_sum);
-    ps[l * E + j] = p;
-  }
-  h = row_sum<L>(h);
+  for (int j = 0; j < E; ++j) ps[l * E + j] = e[j] * inv_sum;
 
   // ---- order the entries by id: bitonic network over packed keys
   Key key[E];
@@ -182,28 +196,49 @@ __global__ void __launch_bounds__(PREP_THREADS)
                  : (WIDE ? (((Key)(uint32_t)id[j]) << 32) | (Key)k
                          : (((Key)(uint32_t)id[j]) << LOGN) | (Key)k);
   }
+  // Merge form of the bitonic network: each merge of two ascending runs of
+  // size/2 first compares position i with its mirror i ^ (size - 1), then
+  // half-cleans with strides size/4 .. 1. Every compare-exchange puts the
+  // smaller key at the lower position, so no step depends on a direction
+  // bit: an in-lane exchange is a min and a max, a cross-lane one a shuffle
+  // and a min or a max.
 #pragma unroll
   for (int size = 2; size <= N; size <<= 1) {
+    if (size <= E) {  // mirror inside the lane: slots j and j ^ (size - 1)
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int j = 0; j < E; ++j) {
+        const int jm = j ^ (size - 1);
+        if ((j & (size >> 1)) == 0) {
+          const Key x = key[j], y = key[jm];
+          key[j] = kmin(x, y);
+          key[jm] = kmax(x, y);
+        }
+      }
+    } else {  // mirror in lane l ^ (size / E - 1), slot E - 1 - j
+      const bool lo = (l & (size / (2 * E))) == 0;
+      Key o[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) o[j] = shfl_key(key[E - 1 - j], size / E - 1);
+#pragma unroll
+      for (int j = 0; j < E; ++j)
+        key[j] = lo ? kmin(o[j], key[j]) : kmax(o[j], key[j]);
+    }
+#pragma unroll
+    for (int stride = size >> 2; stride > 0; stride >>= 1) {
       if (stride >= E) {  // partner in lane l ^ (stride / E), same slot
-        const int lo_side = ((l * E) & stride) == 0;
+        const bool lo = (l & (stride / E)) == 0;
 #pragma unroll
         for (int j = 0; j < E; ++j) {
-          const bool asc = (((l * E + j) & size) == 0);
           const Key o = shfl_key(key[j], stride / E);
-          const bool keep_min = (lo_side != 0) == asc;
-          key[j] = keep_min ? (o < key[j] ? o : key[j]) : (o > key[j] ? o : key[j]);
+          key[j] = lo ? kmin(o, key[j]) : kmax(o, key[j]);
         }
       } else {  // partner in this lane, slot j ^ stride
 #pragma unroll
         for (int j = 0; j < E; ++j) {
           if ((j & stride) == 0) {
-            const bool asc = (((l * E + j) & size) == 0);
             const Key x = key[j], y = key[j + stride];
-            const bool swap = asc ? (x > y) : (x < y);
-            key[j] = swap ? y : x;
-            key[j + stride] = swap ? x : y;
+            key[j] = kmin(x, y);
+            key[j + stride] = kmax(x, y);
           }
         }
       }

@@ -291,91 +291,100 @@ __global__ void __launch_bounds__(PREP_THREADS)
 }
 
 constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_WARPS = COMBINE_THREADS / 32;
+constexpr int COMBINE_TOK = 32;  // tokens per block: one per lane
 
-__global__ void __launch_bounds__(COMBINE_THREADS)
-    lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
-                       const float* __restrict__ pd, int nsplit, int T,
-                       const float* __restrict__ ent, const uint8_t* __restrict__ mask,
-                       const int* __restrict__ invmap, float cl2, float inv_tau,
-                       float* __restrict__ lse, float* __restrict__ token_kl,
-                       double* __restrict__ block_sums) {
-  // invmap: token t's row among the partials (-1: masked, never computed:
-  // lse and KL read 0), or nullptr (row t).
-  const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
-  double contrib = 0.0;
-  if (t < T) {
-    const int r = invmap ? invmap[t] : t;
-    float l = 0.f, kl = 0.f;
-    if (r >= 0) {
-      float M = -INFINITY;
-      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + r]);
-      float S = 0.f, D = 0.f;
-      for (int s = 0; s < nsplit; ++s) {
-        const long long o = (long long)s * T + r;
-        S += ps[o] * exp2f((pm[o] - M) * cl2);
-        D += pd[o];
-      }
-      l = M * inv_tau + logf(S);
-      kl = ent[r] - D * inv_tau + l;
-    }
-    lse[t] = l;
-    if (token_kl) token_kl[t] = kl;
-    if (invmap ? r >= 0 : (mask == nullptr || mask[t] != 0)) contrib = (double)kl;
-  }
-  // fixed-shape tree reduction: deterministic
-  __shared__ double red[COMBINE_THREADS];
-  red[threadIdx.x] = contrib;
-  __syncthreads();
-  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) block_sums[blockIdx.x] = red[0];
+// exp2((x - m) * c) for x <= m, exactly 1 when x == m (both -inf included)
+__device__ __forceinline__ float rescale2(float x, float m, float c) {
+  return x == m ? 1.f : exp2f((x - m) * c);
 }
 
-// Mixed loss: per token alpha c KL + (1 - alpha) CE with CE = lse_1 - z_label.
+// lse_combine: per token, merge the vocabulary splits' partials (max m_s,
+// sum_s exp((z - m_s) / tau) over the split, and the teacher-weighted logit
+// sum d_s) into lse and KL, plus one fp64 sum of m_t KL_t per block. A block
+// takes 32 tokens (one per lane); its 8 warps take every 8th split each,
+// with a running max, and warp 0 merges the 8 partials in warp order: the
+// order of every sum is fixed, so results are deterministic. invmap: token
+// t's row among the partials (-1: masked, never computed: lse and KL read 0),
+// or nullptr (row t).
+// MIX adds the temperature-1 sums and the label logit: the per-token loss is
+// kl_w KL + ce_w (lse_1 - z_label).
+template <bool MIX>
 __global__ void __launch_bounds__(COMBINE_THREADS)
-    lse_combine_mix_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
-                           const float* __restrict__ pd, const float* __restrict__ ps1,
-                           const float* __restrict__ pzl, int nsplit, int T,
-                           const float* __restrict__ ent, const uint8_t* __restrict__ mask,
-                           const int* __restrict__ invmap, float cl2, float inv_tau, float kl_w,
-                           float ce_w, float* __restrict__ lse, float* __restrict__ lse1,
-                           float* __restrict__ token_loss, double* __restrict__ block_sums) {
-  const int t = blockIdx.x * COMBINE_THREADS + threadIdx.x;
-  double contrib = 0.0;
-  if (t < T) {
-    const int r = invmap ? invmap[t] : t;
-    float l = 0.f, l1 = 0.f, tok = 0.f;
-    if (r >= 0) {
-      float M = -INFINITY;
-      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pm[(long long)s * T + r]);
-      float S = 0.f, S1 = 0.f, D = 0.f, Z = 0.f;
-      for (int s = 0; s < nsplit; ++s) {
-        const long long o = (long long)s * T + r;
-        S += ps[o] * exp2f((pm[o] - M) * cl2);
-        S1 += ps1[o] * exp2f((pm[o] - M) * 1.4426950408889634f);
-        D += pd[o];
+    lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                       const float* __restrict__ pd, const float* __restrict__ ps1,
+                       const float* __restrict__ pzl, int nsplit, int T,
+                       const float* __restrict__ ent, const uint8_t* __restrict__ mask,
+                       const int* __restrict__ invmap, float cl2, float inv_tau, float kl_w,
+                       float ce_w, float* __restrict__ lse, float* __restrict__ lse1,
+                       float* __restrict__ token_loss, double* __restrict__ block_sums) {
+  constexpr float L2E = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int t = blockIdx.x * COMBINE_TOK + lane;
+  const int r = t < T ? (invmap ? invmap[t] : t) : -1;
+  float M = -INFINITY, S = 0.f, D = 0.f, S1 = 0.f, Z = 0.f;
+  if (r >= 0) {
+#pragma unroll 4
+    for (int s = w; s < nsplit; s += COMBINE_WARPS) {
+      const long long o = (long long)s * T + r;
+      const float m = pm[o];
+      const float nm = fmaxf(M, m);
+      S = S * rescale2(M, nm, cl2) + ps[o] * rescale2(m, nm, cl2);
+      D += pd[o];
+      if (MIX) {
+        S1 = S1 * rescale2(M, nm, L2E) + ps1[o] * rescale2(m, nm, L2E);
         Z += pzl[o];
       }
+      M = nm;
+    }
+  }
+  __shared__ float part[MIX ? 5 : 3][COMBINE_WARPS][COMBINE_TOK];
+  part[0][w][lane] = M;
+  part[1][w][lane] = S;
+  part[2][w][lane] = D;
+  if (MIX) {
+    part[3][w][lane] = S1;
+    part[4][w][lane] = Z;
+  }
+  __syncthreads();
+  if (w != 0) return;
+  double contrib = 0.0;
+  if (t < T) {
+    float l = 0.f, l1 = 0.f, tok = 0.f;
+    if (r >= 0) {
+      M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < COMBINE_WARPS; ++i) M = fmaxf(M, part[0][i][lane]);
+      S = D = S1 = Z = 0.f;
+#pragma unroll
+      for (int i = 0; i < COMBINE_WARPS; ++i) {
+        const float mi = part[0][i][lane];
+        S += part[1][i][lane] * rescale2(mi, M, cl2);
+        D += part[2][i][lane];
+        if (MIX) {
+          S1 += part[3][i][lane] * rescale2(mi, M, L2E);
+          Z += part[4][i][lane];
+        }
+      }
       l = M * inv_tau + logf(S);
-      l1 = M + logf(S1);
       const float kl = ent[r] - D * inv_tau + l;
-      tok = kl_w * kl + ce_w * (l1 - Z);
+      if (MIX) {
+        l1 = M + logf(S1);
+        tok = kl_w * kl + ce_w * (l1 - Z);
+      } else {
+        tok = kl;
+      }
     }
     lse[t] = l;
-    lse1[t] = l1;
+    if (MIX) lse1[t] = l1;
     if (token_loss) token_loss[t] = tok;
     if (invmap ? r >= 0 : (mask == nullptr || mask[t] != 0)) contrib = (double)tok;
   }
-  __shared__ double red[COMBINE_THREADS];
-  red[threadIdx.x] = contrib;
-  __syncthreads();
-  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) block_sums[blockIdx.x] = red[0];
+  // fixed-shape butterfly over the warp: deterministic
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) contrib += __shfl_xor_sync(0xffffffffu, contrib, o);
+  if (lane == 0) block_sums[blockIdx.x] = contrib;
 }
 
 __global__ void __launch_bounds__(1024)
@@ -721,15 +730,16 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
 #undef KDKL_PREP
 }
 
-int combine_blocks(int T) { return (T + COMBINE_THREADS - 1) / COMBINE_THREADS; }
+int combine_blocks(int T) { return (T + COMBINE_TOK - 1) / COMBINE_TOK; }
 
 cudaError_t launch_lse_combine(const float* pm, const float* ps, const float* pd, int nsplit, int T,
                                const float* ent, const uint8_t* mask, const int* invmap,
                                float cl2, float inv_tau, float* lse, float* token_kl,
                                double* block_sums, cudaStream_t stream) {
-  return launch_kernel("lse_combine", lse_combine_kernel, dim3(combine_blocks(T)),
-                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nsplit, T, ent, mask, invmap,
-                       cl2, inv_tau, lse, token_kl, block_sums);
+  return launch_kernel("lse_combine", lse_combine_kernel<false>, dim3(combine_blocks(T)),
+                       dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, nullptr, nullptr, nsplit, T,
+                       ent, mask, invmap, cl2, inv_tau, 1.f, 0.f, lse, nullptr, token_kl,
+                       block_sums);
 }
 
 cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float* pd,
@@ -738,7 +748,7 @@ cudaError_t launch_lse_combine_mix(const float* pm, const float* ps, const float
                                    float cl2, float inv_tau, float kl_w, float ce_w, float* lse,
                                    float* lse1, float* token_loss, double* block_sums,
                                    cudaStream_t stream) {
-  return launch_kernel("lse_combine_mix", lse_combine_mix_kernel, dim3(combine_blocks(T)),
+  return launch_kernel("lse_combine_mix", lse_combine_kernel<true>, dim3(combine_blocks(T)),
                        dim3(COMBINE_THREADS), 0, stream, pm, ps, pd, ps1, pzl, nsplit, T, ent,
                        mask, invmap, cl2, inv_tau, kl_w, ce_w, lse, lse1, token_loss, block_sums);
 }

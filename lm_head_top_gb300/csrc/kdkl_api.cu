@@ -277,7 +277,9 @@ FwdPlan plan_forward(const kd_kl_problem& p, int num_sms, bool pair, int procs, 
 }
 
 // Block plans of the backward over the tokens x vocabulary plane, each block
-// within the chunk x V budget of the bf16 gradient-of-logits buffer.
+// within the chunk x V budget of the bf16 gradient-of-logits buffer (up to
+// 255 columns over it: vocabulary blocks are whole 256-wide tiles, so that
+// only the last block has a partial tile in the logits and dW GEMMs).
 //   slabs:  all tokens x a vocabulary slab (T <= V), or chunk tokens x all
 //           vocabulary (T > V);
 //   2D:     about sqrt(budget) tokens x the vocabulary that fits.
@@ -296,7 +298,7 @@ BlockPlan slab_plan(const kd_kl_problem& p, int64_t T, double budget) {
     int64_t vb_max = (int64_t)std::min<double>((double)p.V, std::floor(budget / (double)T));
     vb_max = std::max<int64_t>(vb_max, 256);
     b.n_vblocks = ceil_div(p.V, vb_max);
-    b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), 64), p.V);
+    b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), LOGIT_BN), p.V);
     b.n_vblocks = ceil_div(p.V, b.Vb);
     b.n_tblocks = 1;
   } else {
@@ -317,7 +319,7 @@ BlockPlan square_plan(const kd_kl_problem& p, int64_t T, double budget) {
   int64_t vb_max = (int64_t)std::min<double>((double)p.V, std::floor(budget / (double)b.Tb));
   vb_max = std::max<int64_t>(vb_max, 256);
   b.n_vblocks = ceil_div(p.V, vb_max);
-  b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), 64), p.V);
+  b.Vb = std::min<int64_t>(round_up(ceil_div(p.V, b.n_vblocks), LOGIT_BN), p.V);
   b.n_vblocks = ceil_div(p.V, b.Vb);
   return b;
 }

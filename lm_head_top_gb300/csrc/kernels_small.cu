@@ -573,7 +573,7 @@ __device__ int merge_select_k(unsigned long long* keys, int m, int K) {
     const int i = i0 + lane;
     const unsigned long long k = i < m ? keys[i] : ~0ull;
     const bool keep = i < m && k <= cut;
-    const uint32_t mask = __ballot_sync(0xffffffffu, keep);  // all reads of this round are done
+    const uint32_t mask = __ballot_sync(0xffffffffu, keep);  // this pass of 32 has read its keys
     if (keep) keys[w + __popc(mask & below)] = k;
     w += __popc(mask);
   }

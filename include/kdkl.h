@@ -67,8 +67,10 @@ typedef struct {
   float temperature;  /* tau > 0; divides both student and teacher logits */
   int64_t chunk;      /* token-chunk size of the pages' method: bounds the
                          backward's gradient-of-logits buffer to chunk x V
-                         bf16 elements (the scheduler may tile that budget as
-                         fewer tokens x more vocabulary; results are the same) */
+                         bf16 elements, plus tile padding (the scheduler may
+                         tile that budget as fewer tokens x more vocabulary,
+                         in whole 256-wide vocabulary tiles; results are the
+                         same) */
 } kd_kl_problem;
 
 /* Workspace bytes for kd_kl_forward (which = 0), kd_kl_backward (which = 1),
@@ -103,8 +105,9 @@ kd_status kd_kl_forward(const kd_kl_problem* prob, const uint16_t* H, const uint
  *   dH         [T, d] bf16 out    overwritten; fp32 accumulation inside, masked rows = 0
  *   dW         [V, d] fp32 out    overwritten, or added to when accumulate_dW != 0
  * Each logit tile is recomputed and turned into (softmax - P) in the GEMM
- * epilogue; the result is kept in a bf16 buffer of at most chunk x V
- * elements that feeds the dH and dW tensor-core GEMMs. */
+ * epilogue; the result is kept in a bf16 buffer of about chunk x V elements
+ * (the block's vocabulary rounded up to whole 256-wide tiles) that feeds the
+ * dH and dW tensor-core GEMMs. */
 kd_status kd_kl_backward(const kd_kl_problem* prob, const uint16_t* H, const uint16_t* W,
                          const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
                          const float* lse, float grad_loss,

@@ -943,18 +943,18 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
       ep_dw.out_rows = cols;
       ep_dw.out_cols = d;
       ep_dw.accumulate = (accumulate_dW || tb > 0) ? 1 : 0;
-      // One launch pays when a separate one would leave much of its last wave
-      // idle (wave efficiency < 0.9: e.g. dW of narrow vocabulary slabs); the
-      // job with the longer units goes first. Otherwise two launches, which
-      // measured faster (their units start together and share operand tiles
-      // in L2; 45.7 vs 47.4 ms per step at 16K tokens of the GPT-OSS-like head).
-      auto wave_eff = [&](int units) {
-        const double w = (double)units / procs;
-        return w / std::ceil(w);
-      };
+      // One launch pays only when both jobs are small (together at most two
+      // waves of units): it saves a launch and a tail where each is a large
+      // share of the work; the job with the longer units goes first. Otherwise
+      // two launches, which measured faster even with a partial last wave
+      // (their units start together and share operand tiles in L2): 15.6-15.8
+      // vs 16.1-16.5 ms per step for 8K tokens of the Llama-3B-like head, whose
+      // dH has 5.05 waves; 54.1-54.4 vs 54.7-55.0 ms for the padded 4 x 8K
+      // batch at chunk 512; 45.7 vs 47.4 ms at 16K tokens of the GPT-OSS-like
+      // head. At 256 tokens one launch is faster (0.283 vs 0.335 ms per step).
       const char* dual_env = getenv("KDKL_DUAL_DHDW");  // 1: always one launch, 0: never
       const bool dual = dual_env ? dual_env[0] == '1'
-                                 : (std::min(wave_eff(sh_dw.units), wave_eff(sh_dh.units)) < 0.9);
+                                 : ((int64_t)sh_dw.units + sh_dh.units <= 2 * (int64_t)procs);
       if (!dual) {
         sh_dh.counter = next_counter();
         int grid = cta_per_proc * (int)std::min<int64_t>(sh_dh.units, procs);

@@ -259,3 +259,26 @@ def test_narrow_last_column_tile(kdkl, shape, monkeypatch):
     for key in ("dH", "dW"):
         assert np.array_equal(runs["0"][key], runs["1"][key]), key
     _compare(runs["1"], x, w.tau, grad_loss=0.5)
+
+
+@pytest.mark.parametrize("shape", [
+    # T, d, V, K, chunk: vocabulary slabs whose dW and dH jobs are a few waves
+    (700, 320, 9000, 16, 300),
+    (200, 72, 3000, 8, 100),
+])
+def test_dual_and_separate_dh_dw_launches_agree(kdkl, shape, monkeypatch):
+    """dW and dH of a block run as one launch (both jobs' units in one
+    sequence) or as two; each output element sums the same products in the
+    same order either way, so the two give the same bits, and the oracle's
+    results."""
+    T, d, V, K, chunk = shape
+    w = WORKLOADS["small"].with_(T=T, d=d, V=V, K=K, chunk=chunk, tau=1.3,
+                                 seq_len=max(T // 4, 1), pad_frac=0.15)
+    x = make_inputs(w, seed=33)
+    runs = {}
+    for dual in ("0", "1"):
+        monkeypatch.setenv("KDKL_DUAL_DHDW", dual)
+        runs[dual] = run_gpu(kdkl, x, w.tau, w.chunk, grad_loss=0.8)
+    for key in ("dH", "dW"):
+        assert np.array_equal(runs["0"][key], runs["1"][key]), key
+    _compare(runs["0"], x, w.tau, grad_loss=0.8)

@@ -890,11 +890,11 @@ static kd_status backward_impl(const kd_kl_problem* prob, const kd_kl_options* o
         KD_CUDA(launch_gemm(mix ? GEMM_BWD_GRAD_MIX : GEMM_BWD_GRAD, LOGIT_BN, pair, tmH_K, tmW_K,
                             sh, ep, status, grid, stream));
       }
-      // 2) dH[rows] (+)= G . W[cols] and 3) dW[cols] (+)= G^T . H[rows]: one
-      // launch whose units run dW's (long: K = the block's tokens) first, then
-      // dH's (short: K = the slab's columns), so the short units fill the
-      // tail of the long ones. Each output element still gets one store or
-      // one add per launch, in stream order: deterministic.
+      // 2) dH[rows] (+)= G . W[cols] and 3) dW[cols] (+)= G^T . H[rows]: two
+      // launches, or for small blocks one whose units run the job with the
+      // longer units first, so the short ones fill its tail. Each output
+      // element still gets one store or one add per launch, in stream order:
+      // deterministic.
       CUtensorMap tmG_K, tmG_MN;
       if (!encode_bf16_2d(&tmG_K, Gbuf, cols, rows, b.Vb_pad, BK, BM) ||
           !encode_bf16_2d(&tmG_MN, Gbuf, cols, rows, b.Vb_pad, 64, BK))

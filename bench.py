@@ -14,6 +14,7 @@ oracle on bounded token samples of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -562,7 +563,8 @@ def run_kdkl(args):
 
 def run_topk(args):
     """The offline top-K cache producer on the same head shapes: the teacher's
-    K = 100 largest logits per token over V = 201,088 (no logit grid stored)."""
+    K = 100 (or --K) largest logits per token over V = 201,088 (no logit grid
+    stored)."""
     from lm_head_top_gb300 import kdkl
     from lm_head_top_gb300.inputs import WORKLOADS, make_inputs
 
@@ -576,7 +578,7 @@ def run_topk(args):
     if args.tokens:
         w = w.with_(T=args.tokens)
     x = make_inputs(w, seed=args.seed + rank)
-    T, d, V, K = w.T, w.d, w.V, 100
+    T, d, V, K = w.T, w.d, w.V, (args.K or 100)
     torch.cuda.reset_peak_memory_stats(dev)
     H, W = x["H"].to(dev), x["W"].to(dev)
     ws = torch.empty(kdkl.kd_lmhead_topk_workspace_size(T, d, V, K), dtype=torch.uint8, device=dev)
@@ -633,21 +635,21 @@ def run_topk(args):
         return None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(oracle_topk_sample_step, oracle_arrays(x), w, args.cpu_tokens // 2,
-                           "top-%d (dense logit rows, ordered selection)" % K)
+        cpu = cpu_baseline(functools.partial(oracle_topk_sample_step, K=K), oracle_arrays(x), w,
+                           args.cpu_tokens // 2, "top-%d (dense logit rows, ordered selection)" % K)
     pk, pk_src = peaks()
     rows = {n: (c, ms) for n, c, ms in per_kernel}
     c, ms = rows["topk_gemm"]
     flops = 2.0 * T * V * d
     achieved = flops / (ms / c / 1e3) / 1e12  # one topk_gemm launch per step
     return {
-        "metric": "offline top-K teacher cache (LM head x top-100) tokens/s", "path": "topk",
+        "metric": "offline top-K teacher cache (LM head x top-%d) tokens/s" % K, "path": "topk",
         "value": round(T * world * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(elapsed_ms / args.steps, 3), "ms_per_step_median": med_ms,
         "ms_per_step_min": min_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s_topk" % w.name, "T": T, "d": d, "V": V, "K": K,
+        "config": {"workload": "%s_topk%s" % (w.name, "" if K == 100 else "_K%d" % K), "T": T, "d": d, "V": V, "K": K,
                    "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * d * 2 / 1e9)},
         "tflops": round(flops * args.steps / (elapsed_ms / 1e3) / 1e12, 1),
         "peak_hbm_gib": round(torch.cuda.max_memory_allocated(dev) / 2 ** 30, 3),

@@ -368,14 +368,17 @@ constexpr int kTopkMergeMax = 4096;
 // smaller lists also leave more of L2 to the operand tiles.
 constexpr int kTopkSlackDefault = 256;
 
-// Candidate-list room above K before a row's list is compacted (at least 64;
-// the list holds at most 512). Smaller slack compacts more often and raises
-// the shared thresholds sooner, larger slack compacts less often;
+// Candidate-list room above K before a row's list is compacted (64 to 512;
+// the list holds at most 1024). Smaller slack compacts more often and raises
+// the shared thresholds sooner, larger slack compacts less often. Above
+// K = 256 the compactions cost more than the thresholds gain and the slack
+// doubles: K = 512 took 32.0-32.6 ms per 32K tokens with 512 against
+// 34.2-35.1 with 256 (K = 256: 28.2 with 256 against 29.5 with 512).
 // KDKL_TOPK_SLACK overrides the default (tuning).
-int topk_slack() {
+int topk_slack(int K) {
   const char* v = getenv("KDKL_TOPK_SLACK");
   int s = v ? atoi(v) : 0;
-  if (s <= 0) s = kTopkSlackDefault;
+  if (s <= 0) s = K > 256 ? 2 * kTopkSlackDefault : kTopkSlackDefault;
   return std::max(64, std::min(512, s));
 }
 
@@ -413,7 +416,7 @@ TopkPlan plan_topk(const kd_topk_problem& p, int num_sms, bool pair, int procs) 
   f.nsplit = lp.nsplit;
   f.group_m = lp.group_m;
   f.grid = (pair ? 2 : 1) * (int)std::min<int64_t>((int64_t)f.m_tiles * f.nsplit, procs);
-  f.cap = std::max(p.K + 64, std::min(1024, p.K + topk_slack()));
+  f.cap = std::max(p.K + 64, std::min(1024, p.K + topk_slack(p.K)));
   // two list banks per (CTA, row), any grid <= SMs
   const size_t cand = (size_t)num_sms * BM * 2 * f.cap;
   const size_t unit = (size_t)f.nsplit * p.T * p.K;
